@@ -1,0 +1,145 @@
+"""float64 CPU oracle for the Kimi Delta Attention (KDA) recurrence.
+
+TEST INFRASTRUCTURE, NOT PRODUCT CODE.  Only ``tests/``, the smoke check in
+``__graft_entry__`` and the CPU-baseline / reference legs of ``bench.py`` may
+import this package.  It shares no code with the CUDA library
+(``gated_delta_rule_05_gb300``) and never imports it.
+
+The arithmetic lives in ``kda_oracle.c`` (plain C, float64, libm ``exp``); this
+module only compiles it with gcc and marshals numpy arrays through ctypes.
+
+Source of the method: "[논문 리뷰] Kimi K3 Technical Report" (jw9603.github.io),
+sections 3.2 (update and readout), 3.3 (delta form), 3.5 (alpha = exp(g)).
+
+Every function here is pinned by ``tests/test_oracle_pins.py`` (see the list in
+the C file's header); no function is "parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "kda_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "libkda_oracle.so")
+
+_lock = threading.Lock()
+_lib = None
+
+_f64p = ctypes.POINTER(ctypes.c_double)
+_i64p = ctypes.POINTER(ctypes.c_int64)
+
+
+def compile_library(src: str = _SRC, out: str = _LIB_PATH) -> str:
+    """Compile the C oracle into a shared library (IEEE float64, no fast-math)."""
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    tmp = out + ".tmp%d" % os.getpid()
+    cmd = ["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-pthread",
+           "-fno-fast-math", "-ffp-contract=off", src, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def build(force: bool = False) -> str:
+    """Build the oracle library if it is missing or older than its source."""
+    if (force or not os.path.exists(_LIB_PATH)
+            or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC)):
+        compile_library()
+    return _LIB_PATH
+
+
+def _declare(lib):
+    lib.kda_oracle_prefill.restype = ctypes.c_int
+    lib.kda_oracle_prefill.argtypes = [
+        _f64p, _f64p, _f64p, _f64p, _f64p, _f64p, _i64p,
+        ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+        _f64p, _f64p, ctypes.c_int]
+    lib.kda_oracle_decode_step.restype = ctypes.c_int
+    lib.kda_oracle_decode_step.argtypes = [
+        _f64p, _f64p, _f64p, _f64p, _f64p, _f64p,
+        ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+        _f64p, ctypes.c_int]
+    return lib
+
+
+def load_library(path: str):
+    """Load an oracle library from an explicit path (used by the mutant test)."""
+    return _declare(ctypes.CDLL(path))
+
+
+def _get():
+    global _lib
+    with _lock:
+        if _lib is None:
+            _lib = load_library(build())
+        return _lib
+
+
+def _c64(a):
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(_f64p)
+
+
+def default_threads() -> int:
+    return max(1, os.cpu_count() or 1)
+
+
+def prefill(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None,
+            nthreads: int | None = None, lib=None):
+    """Run the recurrence over packed sequences.
+
+    q, k, log_alpha: [T_tot, H, dk]; v: [T_tot, H, dv]; beta: [T_tot, H];
+    S0: [N, H, dk, dv] or None (zeros); cu_seqlens: [N+1] or None (one
+    sequence of all T_tot tokens).  Inputs are widened to float64 exactly.
+    Returns (o [T_tot, H, dv], S_final [N, H, dk, dv]) as float64 arrays.
+    """
+    lib = lib or _get()
+    q, k, v, g, b = (_c64(x) for x in (q, k, v, log_alpha, beta))
+    T, H, dk = q.shape
+    dv = v.shape[2]
+    if cu_seqlens is None:
+        cu = np.array([0, T], dtype=np.int64)
+    else:
+        cu = np.ascontiguousarray(cu_seqlens, dtype=np.int64)
+    N = cu.shape[0] - 1
+    if int(cu[-1]) != T:
+        raise ValueError("cu_seqlens[-1] must equal the number of tokens")
+    s0 = None if S0 is None else _c64(S0)
+    if s0 is not None and s0.shape != (N, H, dk, dv):
+        raise ValueError("S0 must have shape [N, H, dk, dv]")
+    o = np.empty((T, H, dv), dtype=np.float64)
+    S_final = np.empty((N, H, dk, dv), dtype=np.float64)
+    rc = lib.kda_oracle_prefill(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(b), _ptr(s0),
+        cu.ctypes.data_as(_i64p), N, H, dk, dv, _ptr(o), _ptr(S_final),
+        nthreads or default_threads())
+    if rc != 0:
+        raise ValueError("kda_oracle_prefill rejected its arguments (rc=%d)" % rc)
+    return o, S_final
+
+
+def decode_step(q, k, v, log_alpha, beta, S, nthreads: int | None = None,
+                lib=None):
+    """One token per sequence.  q, k, log_alpha: [N, H, dk]; v: [N, H, dv];
+    beta: [N, H]; S: [N, H, dk, dv].  Returns (o [N, H, dv], S_new)."""
+    lib = lib or _get()
+    q, k, v, g, b = (_c64(x) for x in (q, k, v, log_alpha, beta))
+    N, H, dk = q.shape
+    dv = v.shape[2]
+    S_new = np.array(S, dtype=np.float64, copy=True, order="C")
+    o = np.empty((N, H, dv), dtype=np.float64)
+    rc = lib.kda_oracle_decode_step(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(b), _ptr(S_new),
+        N, H, dk, dv, _ptr(o), nthreads or default_threads())
+    if rc != 0:
+        raise ValueError("kda_oracle_decode_step rejected its arguments (rc=%d)" % rc)
+    return o, S_new
