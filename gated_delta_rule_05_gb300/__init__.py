@@ -1,0 +1,183 @@
+"""Python binding of libkda.so, the KDA recurrence library for GB300 (sm_103a).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels behind the C ABI of ``include/kda.h``.  PyTorch is used for device
+memory and streams.  There is no CPU or PyTorch fallback: if the library is
+not built, every call raises.
+
+Functions (same names as the C ABI):
+  kda_prefill(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, ...)
+  kda_decode_step(q, k, v, log_alpha, beta, S_inout, ...)
+  kda_prefill_workspace_bytes(num_seqs, H, d_k, d_v)
+  kda_status_string(code)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from ._build import LIB_PATH, build  # noqa: F401  (re-exported)
+
+KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_WORKSPACE, KDA_ERR_CUDA = range(5)
+KDA_BF16, KDA_FP32 = 0, 1
+
+# Every symbol include/kda.h declares.
+EXPORTS = ("kda_prefill_workspace_bytes", "kda_prefill", "kda_decode_step",
+           "kda_status_string")
+
+
+class KdaError(RuntimeError):
+    def __init__(self, code, where):
+        self.code = code
+        super().__init__("%s: %s" % (where, kda_status_string(code)))
+
+
+_lock = threading.Lock()
+_lib = None
+
+_vp = ctypes.c_void_p
+_i32 = ctypes.c_int32
+_i64 = ctypes.c_int64
+_sz = ctypes.c_size_t
+
+
+def _declare(lib):
+    lib.kda_prefill_workspace_bytes.restype = _sz
+    lib.kda_prefill_workspace_bytes.argtypes = [_i32, _i32, _i32, _i32]
+    lib.kda_prefill.restype = ctypes.c_int
+    lib.kda_prefill.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                _i32, _i64, _i32, _i32, _i32, ctypes.c_int,
+                                _vp, _vp, _vp, _sz, _vp]
+    lib.kda_decode_step.restype = ctypes.c_int
+    lib.kda_decode_step.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp,
+                                    _i32, _i32, _i32, _i32, ctypes.c_int, _vp, _vp]
+    lib.kda_status_string.restype = ctypes.c_char_p
+    lib.kda_status_string.argtypes = [ctypes.c_int]
+    return lib
+
+
+def lib():
+    """The loaded libkda.so (ctypes handle).  Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    "libkda.so is not built (%s); run "
+                    "`python -m gated_delta_rule_05_gb300._build`" % LIB_PATH)
+            _lib = _declare(ctypes.CDLL(LIB_PATH))
+        return _lib
+
+
+def kda_status_string(code: int) -> str:
+    return lib().kda_status_string(int(code)).decode()
+
+
+def kda_prefill_workspace_bytes(num_seqs: int, H: int, d_k: int, d_v: int) -> int:
+    return int(lib().kda_prefill_workspace_bytes(num_seqs, H, d_k, d_v))
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t):
+    torch = _torch()
+    if t.dtype == torch.bfloat16:
+        return KDA_BF16
+    if t.dtype == torch.float32:
+        return KDA_FP32
+    raise TypeError("q/k/v must be bfloat16 or float32, got %s" % t.dtype)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check_cuda(name, t, dtype=None):
+    if t is None:
+        return
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+
+
+def _stream_handle(stream, device):
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def kda_prefill(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, *,
+                o=None, S_final=None, want_state=True, workspace=None,
+                stream=None):
+    """Chunked KDA prefill over packed sequences (C ABI: kda_prefill).
+
+    q, k, log_alpha: [T, H, d_k]; v: [T, H, d_v]; beta: [T, H];
+    S0: [N, H, d_k, d_v] fp32 or None; cu_seqlens: int32 [N+1] or None.
+    Returns (o, S_final); S_final is None when ``want_state`` is False and no
+    buffer was given.  ``S_final`` may be ``S0`` itself (in-place resume).
+    """
+    torch = _torch()
+    T, H, dk = q.shape
+    dv = v.shape[2]
+    dt = _dtype_code(q)
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _check_cuda(name, t, q.dtype)
+    _check_cuda("log_alpha", log_alpha, torch.float32)
+    _check_cuda("beta", beta, torch.float32)
+    _check_cuda("S0", S0, torch.float32)
+    _check_cuda("cu_seqlens", cu_seqlens, torch.int32)
+    N = 1 if cu_seqlens is None else cu_seqlens.shape[0] - 1
+    dev = q.device
+    if o is None:
+        o = torch.empty((T, H, dv), dtype=q.dtype, device=dev)
+    _check_cuda("o", o, q.dtype)
+    if S_final is None and want_state:
+        S_final = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
+    _check_cuda("S_final", S_final, torch.float32)
+    need = kda_prefill_workspace_bytes(N, H, dk, dv)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    _check_cuda("workspace", workspace)
+    with torch.cuda.device(dev):
+        rc = lib().kda_prefill(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(S0),
+            _ptr(cu_seqlens), N, T, H, dk, dv, dt, _ptr(o), _ptr(S_final),
+            _ptr(workspace), workspace.numel() * workspace.element_size(),
+            _stream_handle(stream, dev))
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_prefill")
+    return o, S_final
+
+
+def kda_decode_step(q, k, v, log_alpha, beta, S_inout, *, o=None, stream=None):
+    """One decode step, state updated in place (C ABI: kda_decode_step).
+
+    q, k, log_alpha: [N, H, d_k]; v: [N, H, d_v]; beta: [N, H];
+    S_inout: [N, H, d_k, d_v] fp32.  Returns o [N, H, d_v].
+    """
+    torch = _torch()
+    N, H, dk = q.shape
+    dv = v.shape[2]
+    dt = _dtype_code(q)
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _check_cuda(name, t, q.dtype)
+    _check_cuda("log_alpha", log_alpha, torch.float32)
+    _check_cuda("beta", beta, torch.float32)
+    _check_cuda("S_inout", S_inout, torch.float32)
+    if o is None:
+        o = torch.empty((N, H, dv), dtype=q.dtype, device=q.device)
+    _check_cuda("o", o, q.dtype)
+    with torch.cuda.device(q.device):
+        rc = lib().kda_decode_step(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(S_inout),
+            N, H, dk, dv, dt, _ptr(o), _stream_handle(stream, q.device))
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_decode_step")
+    return o

@@ -1,0 +1,111 @@
+// kda_api.cu -- the C ABI declared in include/kda.h: argument validation,
+// dispatch to the kernels, status mapping.  No allocation, no host sync.
+#include <stdint.h>
+
+#include "kda_internal.cuh"
+
+namespace {
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool supported_d(int32_t d) { return d == 16 || d == 32 || d == 64 || d == 128; }
+
+// True when [a, a+na) and [b, b+nb) overlap.
+bool overlaps(const void* a, size_t na, const void* b, size_t nb)
+{
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+size_t elem_bytes(kda_dtype_t t) { return t == KDA_BF16 ? 2 : 4; }
+
+}  // namespace
+
+extern "C" {
+
+size_t kda_prefill_workspace_bytes(int32_t num_seqs, int32_t H, int32_t d_k,
+                                   int32_t d_v)
+{
+    (void)H;
+    (void)d_k;
+    (void)d_v;
+    return kda::workspace_bytes(num_seqs);
+}
+
+kda_status_t kda_prefill(const void* q, const void* k, const void* v,
+                         const float* log_alpha, const float* beta,
+                         const float* S0, const int32_t* cu_seqlens,
+                         int32_t num_seqs, int64_t total_tokens, int32_t H,
+                         int32_t d_k, int32_t d_v, kda_dtype_t dtype, void* o,
+                         float* S_final, void* workspace, size_t workspace_bytes,
+                         cudaStream_t stream)
+{
+    if (dtype != KDA_BF16 && dtype != KDA_FP32) return KDA_ERR_UNSUPPORTED;
+    if (d_k != d_v || !supported_d(d_k)) return KDA_ERR_UNSUPPORTED;
+    if (num_seqs < 1 || H < 1 || total_tokens < 0) return KDA_ERR_INVALID_ARG;
+    if (cu_seqlens == nullptr && num_seqs != 1) return KDA_ERR_INVALID_ARG;
+    // Token offsets are 32-bit in cu_seqlens.
+    if (total_tokens > INT32_MAX) return KDA_ERR_INVALID_ARG;
+    if (total_tokens > 0 && (!q || !k || !v || !log_alpha || !beta || !o))
+        return KDA_ERR_INVALID_ARG;
+    const void* ptrs16[] = {q, k, v, log_alpha, o, S0, S_final};
+    for (const void* p : ptrs16)
+        if (p && !aligned(p, 16)) return KDA_ERR_INVALID_ARG;
+    if (beta && !aligned(beta, 4)) return KDA_ERR_INVALID_ARG;
+    if (cu_seqlens && !aligned(cu_seqlens, 4)) return KDA_ERR_INVALID_ARG;
+    const size_t state_bytes = (size_t)num_seqs * H * d_k * d_v * sizeof(float);
+    if (S0 && S_final && S0 != S_final && overlaps(S0, state_bytes, S_final, state_bytes))
+        return KDA_ERR_INVALID_ARG;
+    if (o && S_final &&
+        overlaps(o, (size_t)total_tokens * H * d_v * elem_bytes(dtype), S_final, state_bytes))
+        return KDA_ERR_INVALID_ARG;
+    const size_t need = kda::workspace_bytes(num_seqs);
+    if (!workspace || workspace_bytes < need || !aligned(workspace, 256))
+        return KDA_ERR_WORKSPACE;
+
+    int32_t* ws = static_cast<int32_t*>(workspace);
+    cudaError_t err = cudaSuccess;
+    if (cu_seqlens) {
+        err = kda::launch_worklist(cu_seqlens, num_seqs, total_tokens, ws, stream);
+        if (err != cudaSuccess) return KDA_ERR_CUDA;
+    }
+    err = kda::launch_prefill_simt(q, k, v, log_alpha, beta, S0, cu_seqlens, num_seqs,
+                                   total_tokens, H, d_k, dtype, o, S_final, ws, stream);
+    return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+kda_status_t kda_decode_step(const void* q, const void* k, const void* v,
+                             const float* log_alpha, const float* beta,
+                             float* S_inout, int32_t N, int32_t H, int32_t d_k,
+                             int32_t d_v, kda_dtype_t dtype, void* o,
+                             cudaStream_t stream)
+{
+    if (dtype != KDA_BF16 && dtype != KDA_FP32) return KDA_ERR_UNSUPPORTED;
+    if (d_k != d_v || !supported_d(d_k)) return KDA_ERR_UNSUPPORTED;
+    if (N < 1 || H < 1) return KDA_ERR_INVALID_ARG;
+    if (!q || !k || !v || !log_alpha || !beta || !S_inout || !o) return KDA_ERR_INVALID_ARG;
+    const void* ptrs16[] = {q, k, v, log_alpha, o, S_inout};
+    for (const void* p : ptrs16)
+        if (!aligned(p, 16)) return KDA_ERR_INVALID_ARG;
+    if (!aligned(beta, 4)) return KDA_ERR_INVALID_ARG;
+    const size_t state_bytes = (size_t)N * H * d_k * d_v * sizeof(float);
+    if (overlaps(o, (size_t)N * H * d_v * elem_bytes(dtype), S_inout, state_bytes))
+        return KDA_ERR_INVALID_ARG;
+    cudaError_t err = kda::launch_decode(q, k, v, log_alpha, beta, S_inout, N, H, d_k,
+                                         dtype, o, stream);
+    return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+const char* kda_status_string(kda_status_t status)
+{
+    switch (status) {
+        case KDA_OK: return "KDA_OK";
+        case KDA_ERR_INVALID_ARG: return "KDA_ERR_INVALID_ARG: invalid argument";
+        case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED: dtype or head size not supported";
+        case KDA_ERR_WORKSPACE: return "KDA_ERR_WORKSPACE: workspace missing, misaligned or too small";
+        case KDA_ERR_CUDA: return "KDA_ERR_CUDA: a CUDA launch failed";
+        default: return "KDA_ERR_UNKNOWN: unknown status code";
+    }
+}
+
+}  // extern "C"

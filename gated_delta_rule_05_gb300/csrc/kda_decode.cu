@@ -1,0 +1,204 @@
+// kda_decode.cu -- one KDA decode step: a fused, bandwidth-bound
+// read-modify-write of the fp32 state.
+//
+// Method: "[논문 리뷰] Kimi K3 Technical Report" (jw9603.github.io), sections
+// 3.2-3.3.  For one (sequence, head) with state S (rows = key channels):
+//     Sbar = Diag(alpha) S,          alpha = exp(log_alpha)
+//     w    = Sbar^T k = S^T (alpha .* k)
+//     p    = Sbar^T q = S^T (alpha .* q)
+//     u    = beta (v - w)
+//     S'   = Sbar + k u^T
+//     o    = S'^T q = p + (k . q) u
+// Decode is bound by the state bytes it streams ("Kimi 모델 분석",
+// rlaope.github.io, section "Decoding이 왜 느린가"): each state element is read
+// once and written once, so one launch moves 8 * d_k * d_v bytes per
+// (sequence, head) plus a few hundred bytes of token inputs.
+//
+// Mapping: one CTA per (sequence, head, value-column slab).  Value columns of
+// S never mix (column j is updated with v_j alone), so a slab is independent.
+// Each thread holds R float4 of its slab in registers between the read and the
+// write; rows are spread over threads so that every warp reads whole 16-byte
+// aligned row segments (fully coalesced 128-bit accesses).  The state is read
+// with the streaming (evict-first) hint and written with streaming stores: it
+// is touched once per step and must not evict the token inputs.
+#include "kda_internal.cuh"
+
+namespace kda {
+namespace {
+
+template <int DK, int DVS, int THREADS>
+struct DecodeShape {
+    static constexpr int kLanesPerRow = DVS / 4;              // float4 per slab row
+    static constexpr int kRowsPerPass = THREADS / kLanesPerRow;
+    static constexpr int kR = DK / kRowsPerPass;              // float4 per thread
+    static constexpr int kWarps = THREADS / 32;
+    static_assert(DVS % 4 == 0 && kLanesPerRow <= 32, "slab width");
+    static_assert(THREADS % kLanesPerRow == 0, "thread count");
+    static_assert(DK % kRowsPerPass == 0, "rows per pass must divide d_k");
+    static_assert(DVS <= THREADS && DK <= THREADS, "one thread per column / row");
+};
+
+template <typename T, int DK, int DVS, int THREADS>
+__global__ void __launch_bounds__(THREADS)
+decode_kernel(const T* __restrict__ q, const T* __restrict__ k,
+              const T* __restrict__ v, const float* __restrict__ log_alpha,
+              const float* __restrict__ beta, float* __restrict__ S,
+              T* __restrict__ o, int dv)
+{
+    using Sh = DecodeShape<DK, DVS, THREADS>;
+    constexpr int LPR = Sh::kLanesPerRow;
+    constexpr int RPP = Sh::kRowsPerPass;
+    constexpr int R = Sh::kR;
+
+    const int nslab = dv / DVS;
+    const int slab = blockIdx.x % nslab;
+    const long long nh = blockIdx.x / nslab;     // sequence * H + head
+    const int tid = threadIdx.x;
+    const int lane = tid & 31, warp = tid >> 5;
+    const int c4 = tid % LPR;                     // float4 column within the slab
+    const int rg = tid / LPR;                     // first row of this thread
+    const int col = slab * DVS + c4 * 4;
+
+    float* Sp = S + nh * (long long)DK * dv;
+
+    // 1. Issue every state load first so that they are all in flight.
+    float4 s[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const int i = rg + r * RPP;
+        s[r] = __ldcs(reinterpret_cast<const float4*>(Sp + (long long)i * dv + col));
+    }
+
+    __shared__ float sh_a[DK], sh_k[DK], sh_ak[DK], sh_aq[DK];
+    __shared__ float sh_red_w[Sh::kWarps][DVS];
+    __shared__ float sh_red_p[Sh::kWarps][DVS];
+    __shared__ float sh_kq[Sh::kWarps];
+    __shared__ float sh_u[DVS];
+
+    // 2. Token inputs: alpha, k, alpha.*k, alpha.*q and the partial k.q.
+    float kq = 0.f;
+    if (tid < DK) {
+        const long long off = nh * DK + tid;
+        const float a = expf(log_alpha[off]);
+        const float kk = ld_f(k + off);
+        const float qq = ld_f(q + off);
+        sh_a[tid] = a;
+        sh_k[tid] = kk;
+        sh_ak[tid] = a * kk;
+        sh_aq[tid] = a * qq;
+        kq = kk * qq;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, off);
+    if (lane == 0) sh_kq[warp] = kq;
+    __syncthreads();
+
+    // 3. Partial column sums of S^T(alpha.*k) and S^T(alpha.*q) over this
+    //    thread's rows, then across lanes that share the same columns.
+    float4 w = make_float4(0.f, 0.f, 0.f, 0.f), p = w;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const int i = rg + r * RPP;
+        const float ak = sh_ak[i], aq = sh_aq[i];
+        w.x = fmaf(ak, s[r].x, w.x); w.y = fmaf(ak, s[r].y, w.y);
+        w.z = fmaf(ak, s[r].z, w.z); w.w = fmaf(ak, s[r].w, w.w);
+        p.x = fmaf(aq, s[r].x, p.x); p.y = fmaf(aq, s[r].y, p.y);
+        p.z = fmaf(aq, s[r].z, p.z); p.w = fmaf(aq, s[r].w, p.w);
+    }
+#pragma unroll
+    for (int off = LPR; off < 32; off <<= 1) {
+        w.x += __shfl_xor_sync(0xffffffffu, w.x, off);
+        w.y += __shfl_xor_sync(0xffffffffu, w.y, off);
+        w.z += __shfl_xor_sync(0xffffffffu, w.z, off);
+        w.w += __shfl_xor_sync(0xffffffffu, w.w, off);
+        p.x += __shfl_xor_sync(0xffffffffu, p.x, off);
+        p.y += __shfl_xor_sync(0xffffffffu, p.y, off);
+        p.z += __shfl_xor_sync(0xffffffffu, p.z, off);
+        p.w += __shfl_xor_sync(0xffffffffu, p.w, off);
+    }
+    if (lane < LPR) {
+        sh_red_w[warp][c4 * 4 + 0] = w.x; sh_red_w[warp][c4 * 4 + 1] = w.y;
+        sh_red_w[warp][c4 * 4 + 2] = w.z; sh_red_w[warp][c4 * 4 + 3] = w.w;
+        sh_red_p[warp][c4 * 4 + 0] = p.x; sh_red_p[warp][c4 * 4 + 1] = p.y;
+        sh_red_p[warp][c4 * 4 + 2] = p.z; sh_red_p[warp][c4 * 4 + 3] = p.w;
+    }
+    __syncthreads();
+
+    // 4. Per value column: u = beta (v - w), o = p + (k.q) u.
+    if (tid < DVS) {
+        float ws = 0.f, ps = 0.f, kqs = 0.f;
+#pragma unroll
+        for (int i = 0; i < Sh::kWarps; ++i) {
+            ws += sh_red_w[i][tid];
+            ps += sh_red_p[i][tid];
+            kqs += sh_kq[i];
+        }
+        const int j = slab * DVS + tid;
+        const long long vo = nh * dv + j;
+        const float u = beta[nh] * (ld_f(v + vo) - ws);
+        st_f(o + vo, fmaf(kqs, u, ps));
+        sh_u[tid] = u;
+    }
+    __syncthreads();
+
+    // 5. S' = Diag(alpha) S + k u^T, streamed back.
+    const float4 u4 = make_float4(sh_u[c4 * 4 + 0], sh_u[c4 * 4 + 1],
+                                  sh_u[c4 * 4 + 2], sh_u[c4 * 4 + 3]);
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const int i = rg + r * RPP;
+        const float a = sh_a[i], kk = sh_k[i];
+        float4 x;
+        x.x = fmaf(a, s[r].x, kk * u4.x);
+        x.y = fmaf(a, s[r].y, kk * u4.y);
+        x.z = fmaf(a, s[r].z, kk * u4.z);
+        x.w = fmaf(a, s[r].w, kk * u4.w);
+        __stcs(reinterpret_cast<float4*>(Sp + (long long)i * dv + col), x);
+    }
+}
+
+template <typename T, int D>
+cudaError_t launch_typed(const void* q, const void* k, const void* v,
+                         const float* g, const float* beta, float* S,
+                         int32_t N, int32_t H, void* o, cudaStream_t stream)
+{
+    // Slab widths and thread counts: 32 KiB of state per CTA at d = 128
+    // (8 float4 per thread), one warp-row pattern per smaller head size.
+    constexpr int DVS = D >= 64 ? 64 : D;
+    constexpr int THREADS = D == 128 ? 256 : (D == 64 ? 128 : (D == 32 ? 64 : 32));
+    const long long blocks = (long long)N * H * (D / DVS);
+    if (blocks <= 0) return cudaSuccess;
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    decode_kernel<T, D, DVS, THREADS><<<(unsigned)blocks, THREADS, 0, stream>>>(
+        static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v),
+        g, beta, S, static_cast<T*>(o), D);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_d(int32_t d, const void* q, const void* k, const void* v,
+                     const float* g, const float* beta, float* S, int32_t N,
+                     int32_t H, void* o, cudaStream_t stream)
+{
+    switch (d) {
+        case 16: return launch_typed<T, 16>(q, k, v, g, beta, S, N, H, o, stream);
+        case 32: return launch_typed<T, 32>(q, k, v, g, beta, S, N, H, o, stream);
+        case 64: return launch_typed<T, 64>(q, k, v, g, beta, S, N, H, o, stream);
+        case 128: return launch_typed<T, 128>(q, k, v, g, beta, S, N, H, o, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const void* q, const void* k, const void* v,
+                          const float* log_alpha, const float* beta, float* S,
+                          int32_t N, int32_t H, int32_t d, kda_dtype_t dtype,
+                          void* o, cudaStream_t stream)
+{
+    if (dtype == KDA_BF16)
+        return launch_d<__nv_bfloat16>(d, q, k, v, log_alpha, beta, S, N, H, o, stream);
+    return launch_d<float>(d, q, k, v, log_alpha, beta, S, N, H, o, stream);
+}
+
+}  // namespace kda

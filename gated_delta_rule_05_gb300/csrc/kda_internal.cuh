@@ -1,0 +1,53 @@
+// kda_internal.cuh -- declarations shared by the library's translation units.
+// Nothing here is part of the public ABI (include/kda.h is).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kda.h"
+
+namespace kda {
+
+// Workspace layout used by kda_prefill (see kda_prefill_workspace_bytes):
+//   byte 0   : int32 work counter (persistent kernels take items from it)
+//   byte 4   : int32 error word (nonzero => cu_seqlens violated its contract)
+//   byte 256 : int32 order[N], sequence indices, longest first
+constexpr size_t kWsHeaderBytes = 256;
+constexpr int kWsCounterWord = 0;
+constexpr int kWsErrorWord = 1;
+// Sequences are ordered longest-first when N <= this; above it the order is
+// the input order (the rank sort is O(N^2) on one CTA).
+constexpr int kMaxSortedSeqs = 2048;
+
+inline size_t workspace_bytes(int32_t num_seqs) {
+    if (num_seqs < 1) return 0;
+    size_t order = ((size_t)num_seqs * sizeof(int32_t) + 255) / 256 * 256;
+    return kWsHeaderBytes + order;
+}
+
+// Scalar load / store helpers for the two I/O dtypes.
+__device__ __forceinline__ float ld_f(const float* p) { return *p; }
+__device__ __forceinline__ float ld_f(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+__device__ __forceinline__ void st_f(float* p, float x) { *p = x; }
+__device__ __forceinline__ void st_f(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
+
+// Launchers (return cudaGetLastError() after enqueueing).
+cudaError_t launch_worklist(const int32_t* cu_seqlens, int32_t num_seqs,
+                            int64_t total_tokens, int32_t* ws, cudaStream_t stream);
+
+cudaError_t launch_decode(const void* q, const void* k, const void* v,
+                          const float* log_alpha, const float* beta, float* S,
+                          int32_t N, int32_t H, int32_t d, kda_dtype_t dtype,
+                          void* o, cudaStream_t stream);
+
+cudaError_t launch_prefill_simt(const void* q, const void* k, const void* v,
+                                const float* log_alpha, const float* beta,
+                                const float* S0, const int32_t* cu_seqlens,
+                                int32_t num_seqs, int64_t total_tokens, int32_t H,
+                                int32_t d, kda_dtype_t dtype, void* o,
+                                float* S_final, const int32_t* ws,
+                                cudaStream_t stream);
+
+}  // namespace kda

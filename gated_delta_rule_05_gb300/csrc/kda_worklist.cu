@@ -1,0 +1,66 @@
+// kda_worklist.cu -- varlen scheduling for prefill: validate cu_seqlens and
+// order the sequences longest-first on the device.
+//
+// Serving stacks hand a packed batch to the attention kernels together with
+// per-request extents ("attention metadata"); building that metadata with many
+// small host-driven ops was itself a measurable cost ("Kimi 모델 분석",
+// rlaope.github.io, section "커널 최적화", the metadata-builder bullet).  Here
+// the whole step is one single-CTA kernel on the caller's stream, with no host
+// round trip:
+//   * checks cu[0] = 0, cu[n] <= cu[n+1], cu[N] = total_tokens;
+//   * writes the error word (0 = valid) and resets the work counter;
+//   * writes order[] = sequence indices sorted by length, longest first (ties
+//     by index), so that work items handed out in order approximate the
+//     longest-processing-time-first schedule.
+#include "kda_internal.cuh"
+
+namespace kda {
+namespace {
+
+constexpr int kThreads = 1024;
+
+__global__ void __launch_bounds__(kThreads)
+worklist_kernel(const int32_t* __restrict__ cu, int32_t N, int64_t total_tokens,
+                int32_t* __restrict__ ws)
+{
+    __shared__ int bad;
+    __shared__ int32_t len[kMaxSortedSeqs];
+    const int tid = threadIdx.x;
+    if (tid == 0) bad = (cu[0] != 0 || (int64_t)cu[N] != total_tokens) ? 1 : 0;
+    __syncthreads();
+    for (int n = tid; n < N; n += kThreads) {
+        const int32_t l = cu[n + 1] - cu[n];
+        if (l < 0) atomicOr(&bad, 1);
+        if (N <= kMaxSortedSeqs) len[n] = l;
+    }
+    __syncthreads();
+    int32_t* order = ws + kWsHeaderBytes / sizeof(int32_t);
+    if (N <= kMaxSortedSeqs) {
+        for (int n = tid; n < N; n += kThreads) {
+            const int32_t ln = len[n];
+            int rank = 0;
+            for (int m = 0; m < N; ++m) {
+                const int32_t lm = len[m];
+                rank += (lm > ln) || (lm == ln && m < n);
+            }
+            order[rank] = n;
+        }
+    } else {
+        for (int n = tid; n < N; n += kThreads) order[n] = n;
+    }
+    if (tid == 0) {
+        ws[kWsCounterWord] = 0;
+        ws[kWsErrorWord] = bad;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_worklist(const int32_t* cu_seqlens, int32_t num_seqs,
+                            int64_t total_tokens, int32_t* ws, cudaStream_t stream)
+{
+    worklist_kernel<<<1, kThreads, 0, stream>>>(cu_seqlens, num_seqs, total_tokens, ws);
+    return cudaGetLastError();
+}
+
+}  // namespace kda

@@ -1,0 +1,131 @@
+/*
+ * kda.h -- C ABI of the KDA (Kimi Delta Attention) recurrence library for
+ * NVIDIA GB300 (sm_103a).  libkda.so exports exactly the functions below.
+ *
+ * The operation (source: "[논문 리뷰] Kimi K3 Technical Report",
+ * jw9603.github.io, section 3.2 "KDA의 핵심 상태 업데이트"; delta form in
+ * section 3.3; alpha = exp(g) in section 3.5).  Per sequence and head, with a
+ * state S in R^{d_k x d_v} whose rows are key channels:
+ *
+ *     S_t = (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1} + beta_t k_t v_t^T
+ *     o_t = S_t^T q_t                  (read after token t's write)
+ *     alpha_t = exp(log_alpha_t)       (per key channel), beta_t a scalar.
+ *
+ * Conventions shared by every call:
+ *  - All pointers are DEVICE pointers unless stated otherwise; the caller
+ *    owns every buffer.  The library allocates nothing and keeps no state
+ *    between calls other than cached device attributes.
+ *  - Work is enqueued on `stream`; no call synchronises the host.  Argument
+ *    errors are returned synchronously before anything is launched; a launch
+ *    failure returns KDA_ERR_CUDA.  Nothing is thrown across the ABI.
+ *  - Tensors are dense, row-major, with the last index fastest:
+ *      q, k, log_alpha : [T_tot, H, d_k]
+ *      v, o            : [T_tot, H, d_v]
+ *      beta            : [T_tot, H]
+ *      states          : [N, H, d_k, d_v]   fp32
+ *    q, k, v, o share one dtype (kda_dtype_t); log_alpha, beta and states are
+ *    always fp32.  Base pointers must be 16-byte aligned.
+ *  - Preconditions that are documented, not checked on the device:
+ *    -5 <= log_alpha <= 0 (the lower-bounded decay of section 3.5); k is
+ *    L2-normalised and q pre-scaled by the caller (the op uses them as given);
+ *    beta is any finite value (beta up to 2 gives a reflection, "Kimi 모델
+ *    분석", rlaope.github.io, section "반사가 계층을 바꿈"); inputs finite.
+ *  - Supported shapes: KDA_FP32 with d_k = d_v in {16, 32, 64, 128};
+ *    KDA_BF16 with d_k = d_v in {16, 32, 64, 128}.  Anything else returns
+ *    KDA_ERR_UNSUPPORTED.
+ */
+#ifndef KDA_H
+#define KDA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = 1,   /* null required pointer, bad count, misalignment */
+    KDA_ERR_UNSUPPORTED = 2,   /* dtype / head size not implemented */
+    KDA_ERR_WORKSPACE = 3,     /* workspace missing, misaligned or too small */
+    KDA_ERR_CUDA = 4           /* a kernel launch failed (cudaGetLastError) */
+} kda_status_t;
+
+typedef enum {
+    KDA_BF16 = 0,              /* q, k, v, o are bfloat16 */
+    KDA_FP32 = 1               /* q, k, v, o are float32  */
+} kda_dtype_t;
+
+/* Bytes of device workspace kda_prefill needs for num_seqs sequences
+ * (the varlen work list: sequences ordered longest first, a work counter and
+ * an error word).  Returns 0 when num_seqs < 1.  H, d_k and d_v are accepted
+ * for forward compatibility and do not change the result today. */
+size_t kda_prefill_workspace_bytes(int32_t num_seqs, int32_t H, int32_t d_k,
+                                   int32_t d_v);
+
+/* Chunked prefill over packed variable-length sequences.
+ *
+ * Computes o_t for every token of every sequence and, optionally, the state
+ * after each sequence's last token.  The chunkwise-parallel form used on the
+ * GPU ("Kimi 모델 분석", section "순환을 GPU에 올리기": chunks of 64 tokens,
+ * intra-chunk matrix products, inter-chunk state carry) gives the same result
+ * as the token-by-token recurrence up to rounding.
+ *
+ *   q, k, v       [T_tot, H, d] in `dtype`
+ *   log_alpha     [T_tot, H, d_k] fp32, g = ln(alpha)
+ *   beta          [T_tot, H] fp32
+ *   S0            [N, H, d_k, d_v] fp32 initial states, or NULL for zeros
+ *   cu_seqlens    device int32 [N+1]: cu[0] = 0, non-decreasing,
+ *                 cu[N] = total_tokens; sequence n owns tokens
+ *                 cu[n] .. cu[n+1]-1.  NULL means one sequence (N must be 1).
+ *                 Empty sequences are allowed (their S_final = S0).
+ *   num_seqs      N >= 1;  total_tokens >= 0;  H >= 1
+ *   o             [T_tot, H, d_v] in `dtype` (written)
+ *   S_final       [N, H, d_k, d_v] fp32, or NULL when not wanted.  May alias
+ *                 S0 exactly (in-place resume); any other overlap is an error
+ *                 the library cannot detect.
+ *   workspace     device buffer of at least kda_prefill_workspace_bytes(...)
+ *                 bytes, 256-byte aligned; its contents are overwritten.  It
+ *                 must not be shared by calls that may run concurrently.
+ *
+ * If cu_seqlens violates its contract the kernels write nothing and set the
+ * 32-bit word at byte offset 4 of the workspace to a nonzero value (it is
+ * cleared to zero by every call that finds cu_seqlens valid).  This is a
+ * device-side flag: reading it needs a synchronisation by the caller.
+ */
+kda_status_t kda_prefill(const void *q, const void *k, const void *v,
+                         const float *log_alpha, const float *beta,
+                         const float *S0, const int32_t *cu_seqlens,
+                         int32_t num_seqs, int64_t total_tokens, int32_t H,
+                         int32_t d_k, int32_t d_v, kda_dtype_t dtype, void *o,
+                         float *S_final, void *workspace,
+                         size_t workspace_bytes, cudaStream_t stream);
+
+/* One decode step for N independent sequences (one new token each): the
+ * recurrence above applied once per (sequence, head), state updated in place.
+ * Decode reads and writes a fixed 2 * 4 * d_k * d_v bytes of fp32 state per
+ * (sequence, head) whatever the context length ("Kimi 모델 분석", section
+ * "Decoding이 왜 느린가"); it is memory-bound.
+ *
+ *   q, k          [N, H, d_k] in `dtype`;  v: [N, H, d_v] in `dtype`
+ *   log_alpha     [N, H, d_k] fp32;  beta: [N, H] fp32
+ *   S_inout       [N, H, d_k, d_v] fp32, read and overwritten with S_t
+ *   o             [N, H, d_v] in `dtype` (written); must not overlap S_inout
+ */
+kda_status_t kda_decode_step(const void *q, const void *k, const void *v,
+                             const float *log_alpha, const float *beta,
+                             float *S_inout, int32_t N, int32_t H, int32_t d_k,
+                             int32_t d_v, kda_dtype_t dtype, void *o,
+                             cudaStream_t stream);
+
+/* A static, human-readable name for a status code (never NULL). */
+const char *kda_status_string(kda_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H */
