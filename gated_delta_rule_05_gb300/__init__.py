@@ -20,7 +20,7 @@ import threading
 from ._build import LIB_PATH, build  # noqa: F401  (re-exported)
 
 KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_WORKSPACE, KDA_ERR_CUDA = range(5)
-KDA_BF16, KDA_FP32 = 0, 1
+KDA_BF16, KDA_FP32, KDA_BF16_F32OUT = 0, 1, 2
 
 # Every symbol include/kda.h declares.
 EXPORTS = ("kda_prefill_workspace_bytes", "kda_prefill", "kda_decode_step",
@@ -83,13 +83,16 @@ def _torch():
     return torch
 
 
-def _dtype_code(t):
+def _dtype_code(t, out_dtype):
+    """The C ABI's dtype code for inputs of t.dtype and an output of out_dtype."""
     torch = _torch()
-    if t.dtype == torch.bfloat16:
+    if t.dtype == torch.bfloat16 and out_dtype == torch.bfloat16:
         return KDA_BF16
-    if t.dtype == torch.float32:
+    if t.dtype == torch.bfloat16 and out_dtype == torch.float32:
+        return KDA_BF16_F32OUT
+    if t.dtype == torch.float32 and out_dtype == torch.float32:
         return KDA_FP32
-    raise TypeError("q/k/v must be bfloat16 or float32, got %s" % t.dtype)
+    raise TypeError("unsupported input/output dtypes %s -> %s" % (t.dtype, out_dtype))
 
 
 def _ptr(t):
@@ -115,18 +118,22 @@ def _stream_handle(stream, device):
 
 def kda_prefill(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, *,
                 o=None, S_final=None, want_state=True, workspace=None,
-                stream=None):
+                stream=None, o_dtype=None):
     """Chunked KDA prefill over packed sequences (C ABI: kda_prefill).
 
     q, k, log_alpha: [T, H, d_k]; v: [T, H, d_v]; beta: [T, H];
     S0: [N, H, d_k, d_v] fp32 or None; cu_seqlens: int32 [N+1] or None.
     Returns (o, S_final); S_final is None when ``want_state`` is False and no
     buffer was given.  ``S_final`` may be ``S0`` itself (in-place resume).
+    ``o_dtype`` (default: o's dtype if given, else q's) may be float32 for
+    bfloat16 inputs.
     """
     torch = _torch()
     T, H, dk = q.shape
     dv = v.shape[2]
-    dt = _dtype_code(q)
+    if o_dtype is None:
+        o_dtype = o.dtype if o is not None else q.dtype
+    dt = _dtype_code(q, o_dtype)
     for name, t in (("q", q), ("k", k), ("v", v)):
         _check_cuda(name, t, q.dtype)
     _check_cuda("log_alpha", log_alpha, torch.float32)
@@ -136,8 +143,8 @@ def kda_prefill(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, *,
     N = 1 if cu_seqlens is None else cu_seqlens.shape[0] - 1
     dev = q.device
     if o is None:
-        o = torch.empty((T, H, dv), dtype=q.dtype, device=dev)
-    _check_cuda("o", o, q.dtype)
+        o = torch.empty((T, H, dv), dtype=o_dtype, device=dev)
+    _check_cuda("o", o, o_dtype)
     if S_final is None and want_state:
         S_final = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
     _check_cuda("S_final", S_final, torch.float32)
@@ -156,7 +163,8 @@ def kda_prefill(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, *,
     return o, S_final
 
 
-def kda_decode_step(q, k, v, log_alpha, beta, S_inout, *, o=None, stream=None):
+def kda_decode_step(q, k, v, log_alpha, beta, S_inout, *, o=None, stream=None,
+                    o_dtype=None):
     """One decode step, state updated in place (C ABI: kda_decode_step).
 
     q, k, log_alpha: [N, H, d_k]; v: [N, H, d_v]; beta: [N, H];
@@ -165,15 +173,17 @@ def kda_decode_step(q, k, v, log_alpha, beta, S_inout, *, o=None, stream=None):
     torch = _torch()
     N, H, dk = q.shape
     dv = v.shape[2]
-    dt = _dtype_code(q)
+    if o_dtype is None:
+        o_dtype = o.dtype if o is not None else q.dtype
+    dt = _dtype_code(q, o_dtype)
     for name, t in (("q", q), ("k", k), ("v", v)):
         _check_cuda(name, t, q.dtype)
     _check_cuda("log_alpha", log_alpha, torch.float32)
     _check_cuda("beta", beta, torch.float32)
     _check_cuda("S_inout", S_inout, torch.float32)
     if o is None:
-        o = torch.empty((N, H, dv), dtype=q.dtype, device=q.device)
-    _check_cuda("o", o, q.dtype)
+        o = torch.empty((N, H, dv), dtype=o_dtype, device=q.device)
+    _check_cuda("o", o, o_dtype)
     with torch.cuda.device(q.device):
         rc = lib().kda_decode_step(
             _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(S_inout),

@@ -17,7 +17,10 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb)
     return x < y + nb && y < x + na;
 }
 
-size_t elem_bytes(kda_dtype_t t) { return t == KDA_BF16 ? 2 : 4; }
+bool valid_dtype(kda_dtype_t t) { return t == KDA_BF16 || t == KDA_FP32 || t == KDA_BF16_F32OUT; }
+
+// Bytes of one element of o.
+size_t out_bytes(kda_dtype_t t) { return t == KDA_BF16 ? 2 : 4; }
 
 }  // namespace
 
@@ -40,7 +43,7 @@ kda_status_t kda_prefill(const void* q, const void* k, const void* v,
                          float* S_final, void* workspace, size_t workspace_bytes,
                          cudaStream_t stream)
 {
-    if (dtype != KDA_BF16 && dtype != KDA_FP32) return KDA_ERR_UNSUPPORTED;
+    if (!valid_dtype(dtype)) return KDA_ERR_UNSUPPORTED;
     if (d_k != d_v || !supported_d(d_k)) return KDA_ERR_UNSUPPORTED;
     if (num_seqs < 1 || H < 1 || total_tokens < 0) return KDA_ERR_INVALID_ARG;
     if (cu_seqlens == nullptr && num_seqs != 1) return KDA_ERR_INVALID_ARG;
@@ -57,7 +60,7 @@ kda_status_t kda_prefill(const void* q, const void* k, const void* v,
     if (S0 && S_final && S0 != S_final && overlaps(S0, state_bytes, S_final, state_bytes))
         return KDA_ERR_INVALID_ARG;
     if (o && S_final &&
-        overlaps(o, (size_t)total_tokens * H * d_v * elem_bytes(dtype), S_final, state_bytes))
+        overlaps(o, (size_t)total_tokens * H * d_v * out_bytes(dtype), S_final, state_bytes))
         return KDA_ERR_INVALID_ARG;
     const size_t need = kda::workspace_bytes(num_seqs);
     if (!workspace || workspace_bytes < need || !aligned(workspace, 256))
@@ -80,7 +83,7 @@ kda_status_t kda_decode_step(const void* q, const void* k, const void* v,
                              int32_t d_v, kda_dtype_t dtype, void* o,
                              cudaStream_t stream)
 {
-    if (dtype != KDA_BF16 && dtype != KDA_FP32) return KDA_ERR_UNSUPPORTED;
+    if (!valid_dtype(dtype)) return KDA_ERR_UNSUPPORTED;
     if (d_k != d_v || !supported_d(d_k)) return KDA_ERR_UNSUPPORTED;
     if (N < 1 || H < 1) return KDA_ERR_INVALID_ARG;
     if (!q || !k || !v || !log_alpha || !beta || !S_inout || !o) return KDA_ERR_INVALID_ARG;
@@ -89,7 +92,7 @@ kda_status_t kda_decode_step(const void* q, const void* k, const void* v,
         if (!aligned(p, 16)) return KDA_ERR_INVALID_ARG;
     if (!aligned(beta, 4)) return KDA_ERR_INVALID_ARG;
     const size_t state_bytes = (size_t)N * H * d_k * d_v * sizeof(float);
-    if (overlaps(o, (size_t)N * H * d_v * elem_bytes(dtype), S_inout, state_bytes))
+    if (overlaps(o, (size_t)N * H * d_v * out_bytes(dtype), S_inout, state_bytes))
         return KDA_ERR_INVALID_ARG;
     cudaError_t err = kda::launch_decode(q, k, v, log_alpha, beta, S_inout, N, H, d_k,
                                          dtype, o, stream);

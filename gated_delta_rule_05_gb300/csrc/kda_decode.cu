@@ -38,12 +38,12 @@ struct DecodeShape {
     static_assert(DVS <= THREADS && DK <= THREADS, "one thread per column / row");
 };
 
-template <typename T, int DK, int DVS, int THREADS>
+template <typename TI, typename TO, int DK, int DVS, int THREADS>
 __global__ void __launch_bounds__(THREADS)
-decode_kernel(const T* __restrict__ q, const T* __restrict__ k,
-              const T* __restrict__ v, const float* __restrict__ log_alpha,
+decode_kernel(const TI* __restrict__ q, const TI* __restrict__ k,
+              const TI* __restrict__ v, const float* __restrict__ log_alpha,
               const float* __restrict__ beta, float* __restrict__ S,
-              T* __restrict__ o, int dv)
+              TO* __restrict__ o, int dv)
 {
     using Sh = DecodeShape<DK, DVS, THREADS>;
     constexpr int LPR = Sh::kLanesPerRow;
@@ -157,7 +157,7 @@ decode_kernel(const T* __restrict__ q, const T* __restrict__ k,
     }
 }
 
-template <typename T, int D>
+template <typename TI, typename TO, int D>
 cudaError_t launch_typed(const void* q, const void* k, const void* v,
                          const float* g, const float* beta, float* S,
                          int32_t N, int32_t H, void* o, cudaStream_t stream)
@@ -169,22 +169,22 @@ cudaError_t launch_typed(const void* q, const void* k, const void* v,
     const long long blocks = (long long)N * H * (D / DVS);
     if (blocks <= 0) return cudaSuccess;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    decode_kernel<T, D, DVS, THREADS><<<(unsigned)blocks, THREADS, 0, stream>>>(
-        static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v),
-        g, beta, S, static_cast<T*>(o), D);
+    decode_kernel<TI, TO, D, DVS, THREADS><<<(unsigned)blocks, THREADS, 0, stream>>>(
+        static_cast<const TI*>(q), static_cast<const TI*>(k), static_cast<const TI*>(v),
+        g, beta, S, static_cast<TO*>(o), D);
     return cudaGetLastError();
 }
 
-template <typename T>
+template <typename TI, typename TO>
 cudaError_t launch_d(int32_t d, const void* q, const void* k, const void* v,
                      const float* g, const float* beta, float* S, int32_t N,
                      int32_t H, void* o, cudaStream_t stream)
 {
     switch (d) {
-        case 16: return launch_typed<T, 16>(q, k, v, g, beta, S, N, H, o, stream);
-        case 32: return launch_typed<T, 32>(q, k, v, g, beta, S, N, H, o, stream);
-        case 64: return launch_typed<T, 64>(q, k, v, g, beta, S, N, H, o, stream);
-        case 128: return launch_typed<T, 128>(q, k, v, g, beta, S, N, H, o, stream);
+        case 16: return launch_typed<TI, TO, 16>(q, k, v, g, beta, S, N, H, o, stream);
+        case 32: return launch_typed<TI, TO, 32>(q, k, v, g, beta, S, N, H, o, stream);
+        case 64: return launch_typed<TI, TO, 64>(q, k, v, g, beta, S, N, H, o, stream);
+        case 128: return launch_typed<TI, TO, 128>(q, k, v, g, beta, S, N, H, o, stream);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -196,9 +196,14 @@ cudaError_t launch_decode(const void* q, const void* k, const void* v,
                           int32_t N, int32_t H, int32_t d, kda_dtype_t dtype,
                           void* o, cudaStream_t stream)
 {
-    if (dtype == KDA_BF16)
-        return launch_d<__nv_bfloat16>(d, q, k, v, log_alpha, beta, S, N, H, o, stream);
-    return launch_d<float>(d, q, k, v, log_alpha, beta, S, N, H, o, stream);
+    switch (dtype) {
+        case KDA_BF16:
+            return launch_d<__nv_bfloat16, __nv_bfloat16>(d, q, k, v, log_alpha, beta, S, N, H, o, stream);
+        case KDA_BF16_F32OUT:
+            return launch_d<__nv_bfloat16, float>(d, q, k, v, log_alpha, beta, S, N, H, o, stream);
+        default:
+            return launch_d<float, float>(d, q, k, v, log_alpha, beta, S, N, H, o, stream);
+    }
 }
 
 }  // namespace kda

@@ -54,13 +54,13 @@ struct SimtSmem {
     static constexpr size_t kBytes = kFloats * sizeof(float);
 };
 
-template <typename T, int DK, int DVS>
+template <typename TI, typename TO, int DK, int DVS>
 __global__ void __launch_bounds__(kThreads)
-prefill_simt_kernel(const T* __restrict__ q, const T* __restrict__ k,
-                    const T* __restrict__ v, const float* __restrict__ g,
+prefill_simt_kernel(const TI* __restrict__ q, const TI* __restrict__ k,
+                    const TI* __restrict__ v, const float* __restrict__ g,
                     const float* __restrict__ beta, const float* S0,
                     const int32_t* __restrict__ cu, const int32_t* __restrict__ ws,
-                    long long total_tokens, int H, T* __restrict__ o,
+                    long long total_tokens, int H, TO* __restrict__ o,
                     float* S_final)   // may alias S0: no __restrict__ on either
 {
     using L = SimtSmem<DK, DVS>;
@@ -213,7 +213,7 @@ prefill_simt_kernel(const T* __restrict__ q, const T* __restrict__ k,
     }
 }
 
-template <typename T, int D>
+template <typename TI, typename TO, int D>
 cudaError_t launch_typed(const void* q, const void* k, const void* v,
                          const float* g, const float* beta, const float* S0,
                          const int32_t* cu, int32_t N, int64_t T_tot, int32_t H,
@@ -222,7 +222,7 @@ cudaError_t launch_typed(const void* q, const void* k, const void* v,
 {
     constexpr int DVS = D < 32 ? D : 32;
     using L = SimtSmem<D, DVS>;
-    auto kern = prefill_simt_kernel<T, D, DVS>;
+    auto kern = prefill_simt_kernel<TI, TO, D, DVS>;
     static bool attr_set = false;   // benign race: every writer stores the same value
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(
@@ -234,12 +234,12 @@ cudaError_t launch_typed(const void* q, const void* k, const void* v,
     if (blocks <= 0) return cudaSuccess;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     kern<<<(unsigned)blocks, kThreads, L::kBytes, stream>>>(
-        static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v),
-        g, beta, S0, cu, ws, (long long)T_tot, H, static_cast<T*>(o), S_final);
+        static_cast<const TI*>(q), static_cast<const TI*>(k), static_cast<const TI*>(v),
+        g, beta, S0, cu, ws, (long long)T_tot, H, static_cast<TO*>(o), S_final);
     return cudaGetLastError();
 }
 
-template <typename T>
+template <typename TI, typename TO>
 cudaError_t launch_d(int32_t d, const void* q, const void* k, const void* v,
                      const float* g, const float* beta, const float* S0,
                      const int32_t* cu, int32_t N, int64_t T_tot, int32_t H,
@@ -247,10 +247,10 @@ cudaError_t launch_d(int32_t d, const void* q, const void* k, const void* v,
                      cudaStream_t stream)
 {
     switch (d) {
-        case 16: return launch_typed<T, 16>(q, k, v, g, beta, S0, cu, N, T_tot, H, o, S_final, ws, stream);
-        case 32: return launch_typed<T, 32>(q, k, v, g, beta, S0, cu, N, T_tot, H, o, S_final, ws, stream);
-        case 64: return launch_typed<T, 64>(q, k, v, g, beta, S0, cu, N, T_tot, H, o, S_final, ws, stream);
-        case 128: return launch_typed<T, 128>(q, k, v, g, beta, S0, cu, N, T_tot, H, o, S_final, ws, stream);
+        case 16: return launch_typed<TI, TO, 16>(q, k, v, g, beta, S0, cu, N, T_tot, H, o, S_final, ws, stream);
+        case 32: return launch_typed<TI, TO, 32>(q, k, v, g, beta, S0, cu, N, T_tot, H, o, S_final, ws, stream);
+        case 64: return launch_typed<TI, TO, 64>(q, k, v, g, beta, S0, cu, N, T_tot, H, o, S_final, ws, stream);
+        case 128: return launch_typed<TI, TO, 128>(q, k, v, g, beta, S0, cu, N, T_tot, H, o, S_final, ws, stream);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -265,11 +265,17 @@ cudaError_t launch_prefill_simt(const void* q, const void* k, const void* v,
                                 float* S_final, const int32_t* ws,
                                 cudaStream_t stream)
 {
-    if (dtype == KDA_BF16)
-        return launch_d<__nv_bfloat16>(d, q, k, v, log_alpha, beta, S0, cu_seqlens,
-                                       num_seqs, total_tokens, H, o, S_final, ws, stream);
-    return launch_d<float>(d, q, k, v, log_alpha, beta, S0, cu_seqlens, num_seqs,
-                           total_tokens, H, o, S_final, ws, stream);
+    switch (dtype) {
+        case KDA_BF16:
+            return launch_d<__nv_bfloat16, __nv_bfloat16>(d, q, k, v, log_alpha, beta, S0, cu_seqlens,
+                                                          num_seqs, total_tokens, H, o, S_final, ws, stream);
+        case KDA_BF16_F32OUT:
+            return launch_d<__nv_bfloat16, float>(d, q, k, v, log_alpha, beta, S0, cu_seqlens,
+                                                  num_seqs, total_tokens, H, o, S_final, ws, stream);
+        default:
+            return launch_d<float, float>(d, q, k, v, log_alpha, beta, S0, cu_seqlens, num_seqs,
+                                          total_tokens, H, o, S_final, ws, stream);
+    }
 }
 
 }  // namespace kda

@@ -23,16 +23,16 @@
  *      v, o            : [T_tot, H, d_v]
  *      beta            : [T_tot, H]
  *      states          : [N, H, d_k, d_v]   fp32
- *    q, k, v, o share one dtype (kda_dtype_t); log_alpha, beta and states are
- *    always fp32.  Base pointers must be 16-byte aligned.
+ *    q, k, v share one dtype and o has the output dtype (kda_dtype_t);
+ *    log_alpha, beta and states are always fp32.  Base pointers must be
+ *    16-byte aligned.
  *  - Preconditions that are documented, not checked on the device:
  *    -5 <= log_alpha <= 0 (the lower-bounded decay of section 3.5); k is
  *    L2-normalised and q pre-scaled by the caller (the op uses them as given);
  *    beta is any finite value (beta up to 2 gives a reflection, "Kimi 모델
  *    분석", rlaope.github.io, section "반사가 계층을 바꿈"); inputs finite.
- *  - Supported shapes: KDA_FP32 with d_k = d_v in {16, 32, 64, 128};
- *    KDA_BF16 with d_k = d_v in {16, 32, 64, 128}.  Anything else returns
- *    KDA_ERR_UNSUPPORTED.
+ *  - Supported shapes: every dtype code with d_k = d_v in {16, 32, 64, 128}.
+ *    Anything else returns KDA_ERR_UNSUPPORTED.
  */
 #ifndef KDA_H
 #define KDA_H
@@ -56,7 +56,8 @@ typedef enum {
 
 typedef enum {
     KDA_BF16 = 0,              /* q, k, v, o are bfloat16 */
-    KDA_FP32 = 1               /* q, k, v, o are float32  */
+    KDA_FP32 = 1,              /* q, k, v, o are float32  */
+    KDA_BF16_F32OUT = 2        /* q, k, v are bfloat16, o is float32 */
 } kda_dtype_t;
 
 /* Bytes of device workspace kda_prefill needs for num_seqs sequences
@@ -74,7 +75,7 @@ size_t kda_prefill_workspace_bytes(int32_t num_seqs, int32_t H, int32_t d_k,
  * intra-chunk matrix products, inter-chunk state carry) gives the same result
  * as the token-by-token recurrence up to rounding.
  *
- *   q, k, v       [T_tot, H, d] in `dtype`
+ *   q, k, v       [T_tot, H, d] in the input dtype of `dtype`
  *   log_alpha     [T_tot, H, d_k] fp32, g = ln(alpha)
  *   beta          [T_tot, H] fp32
  *   S0            [N, H, d_k, d_v] fp32 initial states, or NULL for zeros
@@ -83,7 +84,7 @@ size_t kda_prefill_workspace_bytes(int32_t num_seqs, int32_t H, int32_t d_k,
  *                 cu[n] .. cu[n+1]-1.  NULL means one sequence (N must be 1).
  *                 Empty sequences are allowed (their S_final = S0).
  *   num_seqs      N >= 1;  total_tokens >= 0;  H >= 1
- *   o             [T_tot, H, d_v] in `dtype` (written)
+ *   o             [T_tot, H, d_v] in the output dtype of `dtype` (written)
  *   S_final       [N, H, d_k, d_v] fp32, or NULL when not wanted.  May alias
  *                 S0 exactly (in-place resume); any other overlap is an error
  *                 the library cannot detect.
@@ -110,10 +111,11 @@ kda_status_t kda_prefill(const void *q, const void *k, const void *v,
  * (sequence, head) whatever the context length ("Kimi 모델 분석", section
  * "Decoding이 왜 느린가"); it is memory-bound.
  *
- *   q, k          [N, H, d_k] in `dtype`;  v: [N, H, d_v] in `dtype`
+ *   q, k          [N, H, d_k], v: [N, H, d_v], in the input dtype of `dtype`
  *   log_alpha     [N, H, d_k] fp32;  beta: [N, H] fp32
  *   S_inout       [N, H, d_k, d_v] fp32, read and overwritten with S_t
- *   o             [N, H, d_v] in `dtype` (written); must not overlap S_inout
+ *   o             [N, H, d_v] in the output dtype of `dtype` (written); must
+ *                 not overlap S_inout
  */
 kda_status_t kda_decode_step(const void *q, const void *k, const void *v,
                              const float *log_alpha, const float *beta,

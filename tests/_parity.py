@@ -4,6 +4,13 @@ compare with the error measure the tests use.
 Error measure: max |x_gpu - x_ref| over the compared elements, divided by the
 RMS of x_ref over the same elements.  Tolerances: 2e-2 for bf16 inputs with an
 fp32 state, 1e-4 for fp32 inputs.
+
+A result stored in bfloat16 carries its own rounding, up to half an ulp
+(2^-8 |x| relative) per element; even the exactly rounded oracle value exceeds
+2e-2 x RMS by that alone once max|o| is about 8 x RMS.  For bf16 outputs the
+bound is therefore applied to what the kernel adds beyond that rounding:
+max(|x_gpu - x_ref| - 2^-8 |x_ref|) <= tol x RMS(x_ref).  fp32 results (S_final,
+and o with an fp32 output) are held to the plain bound.
 """
 from __future__ import annotations
 
@@ -20,22 +27,34 @@ def to64(t):
     return t.detach().to("cpu").double().numpy()
 
 
-def rel_err(x, ref):
+BF16_HALF_ULP = 2.0 ** -8
+
+
+def rel_err(x, ref, bf16_out=False):
     x = np.asarray(x, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     assert x.shape == ref.shape, (x.shape, ref.shape)
     if ref.size == 0:
         return 0.0
-    rms = float(np.sqrt(np.mean(ref * ref)))
-    err = float(np.max(np.abs(x - ref)))
     assert np.all(np.isfinite(x)), "non-finite values in the GPU result"
+    rms = float(np.sqrt(np.mean(ref * ref)))
+    d = np.abs(x - ref)
+    if bf16_out:
+        d = d - BF16_HALF_ULP * np.abs(ref)
+    err = float(np.max(d))
     return err / rms if rms > 0 else err
 
 
-def assert_close(x, ref, tol, what=""):
-    e = rel_err(x, ref)
+def assert_close(x, ref, tol, what="", bf16_out=False):
+    e = rel_err(x, ref, bf16_out)
     assert e <= tol, "%s: max|err|/rms = %.3e > %.1e" % (what, e, tol)
     return e
+
+
+def compare_out(o_gpu, ref, tol, what="o"):
+    """Compare an output tensor (bf16 or fp32) with the rule for its dtype."""
+    return assert_close(to64(o_gpu), ref, tol, what,
+                        bf16_out=(o_gpu.dtype == torch.bfloat16))
 
 
 def oracle_prefill(inp, heads=None, cols=None, seg_tokens=None, nthreads=None):

@@ -11,7 +11,7 @@ import pytest
 import torch
 
 import synth
-from tests._parity import TOL, assert_close, oracle_prefill, to64
+from tests._parity import TOL, assert_close, compare_out, oracle_prefill, to64
 
 pytestmark = pytest.mark.gpu
 
@@ -26,22 +26,23 @@ def kda():
     return m
 
 
-def run_prefill(kda, inp, want_state=True):
+def run_prefill(kda, inp, want_state=True, o_dtype=None):
     d = inp.to("cuda")
     o, S = kda.kda_prefill(d.q, d.k, d.v, d.log_alpha, d.beta, S0=d.S0,
-                           cu_seqlens=d.cu_seqlens, want_state=want_state)
+                           cu_seqlens=d.cu_seqlens, want_state=want_state,
+                           o_dtype=o_dtype)
     torch.cuda.synchronize()
     return o, S
 
 
-def check_prefill(kda, inp, dtype, heads=None, cols=None, seg=None):
-    o, S = run_prefill(kda, inp)
+def check_prefill(kda, inp, dtype, heads=None, cols=None, seg=None, o_dtype=None):
+    o, S = run_prefill(kda, inp, o_dtype=o_dtype)
     o_ref, S_ref = oracle_prefill(inp, heads=heads, cols=cols, seg_tokens=seg)
     hi = list(range(inp.q.shape[1])) if heads is None else list(heads)
     ci = list(range(inp.v.shape[2])) if cols is None else list(cols)
     og = o[:, hi][:, :, ci]
     Sg = S[:, hi][:, :, :, ci]
-    e1 = assert_close(to64(og), o_ref, TOL[dtype], "o")
+    e1 = compare_out(og, o_ref, TOL[dtype], "o")
     e2 = assert_close(to64(Sg), S_ref, TOL[dtype], "S_final")
     return e1, e2
 
@@ -56,6 +57,12 @@ def test_recurrent_tiny_fp32(kda):
 def test_prefill_h16_t4096(kda):
     inp = synth.workload_inputs(2, device="cpu")
     check_prefill(kda, inp, "bf16")
+
+
+def test_prefill_h16_t4096_fp32_output(kda):
+    # bf16 inputs, fp32 output: the plain bound, with no output rounding.
+    inp = synth.workload_inputs(2, device="cpu")
+    check_prefill(kda, inp, "bf16", o_dtype=torch.float32)
 
 
 def test_varlen16_h32_sampled_columns(kda):
@@ -80,7 +87,7 @@ def test_decode_1024x32(kda):
     sel = lambda t: to64(t.index_select(0, n))
     o_ref, S_ref = oracle.decode_step(sel(inp.q), sel(inp.k), sel(inp.v),
                                       sel(inp.log_alpha), sel(inp.beta), sel(inp.S0))
-    assert_close(sel(o), o_ref, TOL["bf16"], "o")
+    assert_close(sel(o), o_ref, TOL["bf16"], "o", bf16_out=True)
     assert_close(sel(S), S_ref, TOL["bf16"], "S")
 
 
@@ -144,7 +151,7 @@ def test_resume_in_place(kda):
     torch.cuda.synchronize()
     assert S2.data_ptr() == S.data_ptr()
     o_ref, S_ref = oracle_prefill(inp)
-    assert_close(to64(torch.cat([o1, o2])), o_ref, TOL["bf16"], "o")
+    compare_out(torch.cat([o1, o2]), o_ref, TOL["bf16"], "o")
     assert_close(to64(S), S_ref, TOL["bf16"], "S")
 
 
@@ -159,7 +166,7 @@ def test_decode_chain_equals_prefill(kda):
                                         dv.log_alpha[t:t + 1], dv.beta[t:t + 1], S))
     torch.cuda.synchronize()
     o_ref, S_ref = oracle_prefill(inp)
-    assert_close(to64(torch.cat(outs)), o_ref, TOL["fp32"], "o")
+    compare_out(torch.cat(outs), o_ref, TOL["fp32"], "o")
     assert_close(to64(S), S_ref, TOL["fp32"], "S")
 
 
@@ -174,8 +181,23 @@ def test_decode_head_sizes(kda, d, dtype):
     torch.cuda.synchronize()
     o_ref, S_ref = oracle.decode_step(to64(inp.q), to64(inp.k), to64(inp.v),
                                       to64(inp.log_alpha), to64(inp.beta), to64(inp.S0))
-    assert_close(to64(o), o_ref, TOL[dtype], "o")
+    compare_out(o, o_ref, TOL[dtype], "o")
     assert_close(to64(S), S_ref, TOL[dtype], "S")
+
+
+def test_decode_fp32_output(kda):
+    import oracle
+    inp = synth.generate([1] * 64, 4, 128, 128, dtype="bf16", s0_std=0.02, seed=300)
+    dv = inp.to("cuda")
+    S = dv.S0.clone()
+    o = kda.kda_decode_step(dv.q, dv.k, dv.v, dv.log_alpha, dv.beta, S,
+                            o_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert o.dtype == torch.float32
+    o_ref, S_ref = oracle.decode_step(to64(inp.q), to64(inp.k), to64(inp.v),
+                                      to64(inp.log_alpha), to64(inp.beta), to64(inp.S0))
+    assert_close(to64(o), o_ref, TOL["bf16"], "o")
+    assert_close(to64(S), S_ref, TOL["bf16"], "S")
 
 
 # --- device-side argument check ---------------------------------------------
