@@ -72,8 +72,12 @@ kda_status_t kda_prefill(const void* q, const void* k, const void* v,
         err = kda::launch_worklist(cu_seqlens, num_seqs, total_tokens, ws, stream);
         if (err != cudaSuccess) return KDA_ERR_CUDA;
     }
-    err = kda::launch_prefill_simt(q, k, v, log_alpha, beta, S0, cu_seqlens, num_seqs,
-                                   total_tokens, H, d_k, dtype, o, S_final, ws, stream);
+    if (kda::prefill_tc_supported(dtype, d_k, total_tokens))
+        err = kda::launch_prefill_tc(q, k, v, log_alpha, beta, S0, cu_seqlens, num_seqs,
+                                     total_tokens, H, dtype, o, S_final, ws, stream);
+    else
+        err = kda::launch_prefill_simt(q, k, v, log_alpha, beta, S0, cu_seqlens, num_seqs,
+                                       total_tokens, H, d_k, dtype, o, S_final, ws, stream);
     return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 

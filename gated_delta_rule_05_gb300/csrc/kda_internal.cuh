@@ -5,6 +5,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <stdlib.h>
 
 #include "kda.h"
 
@@ -13,10 +14,12 @@ namespace kda {
 // Workspace layout used by kda_prefill (see kda_prefill_workspace_bytes):
 //   byte 0   : int32 work counter (persistent kernels take items from it)
 //   byte 4   : int32 error word (nonzero => cu_seqlens violated its contract)
+//   byte 8   : int32 timeout word (bit 1 set => a device-side wait gave up)
 //   byte 256 : int32 order[N], sequence indices, longest first
 constexpr size_t kWsHeaderBytes = 256;
 constexpr int kWsCounterWord = 0;
 constexpr int kWsErrorWord = 1;
+constexpr int kWsTimeoutWord = 2;
 // Sequences are ordered longest-first when N <= this; above it the order is
 // the input order (the rank sort is O(N^2) on one CTA).
 constexpr int kMaxSortedSeqs = 2048;
@@ -26,6 +29,10 @@ inline size_t workspace_bytes(int32_t num_seqs) {
     size_t order = ((size_t)num_seqs * sizeof(int32_t) + 255) / 256 * 256;
     return kWsHeaderBytes + order;
 }
+
+// KDA_DEBUG set in the environment: failing host-side steps are reported on
+// stderr (the status codes stay the same).
+inline bool debug_enabled() { return getenv("KDA_DEBUG") != nullptr; }
 
 // Scalar load / store helpers for the two I/O dtypes.
 __device__ __forceinline__ float ld_f(const float* p) { return *p; }
@@ -49,5 +56,16 @@ cudaError_t launch_prefill_simt(const void* q, const void* k, const void* v,
                                 int32_t d, kda_dtype_t dtype, void* o,
                                 float* S_final, const int32_t* ws,
                                 cudaStream_t stream);
+
+// Tensor-core prefill (bf16 q/k/v, d = 128).  Returns false when the call
+// must take the CUDA-core path instead (other dtypes or head sizes, no tokens,
+// or KDA_FORCE_SIMT set in the environment).
+bool prefill_tc_supported(kda_dtype_t dtype, int32_t d, int64_t total_tokens);
+
+cudaError_t launch_prefill_tc(const void* q, const void* k, const void* v,
+                              const float* log_alpha, const float* beta, const float* S0,
+                              const int32_t* cu_seqlens, int32_t num_seqs, int64_t total_tokens,
+                              int32_t H, kda_dtype_t dtype, void* o, float* S_final,
+                              int32_t* ws, cudaStream_t stream);
 
 }  // namespace kda

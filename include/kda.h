@@ -94,8 +94,18 @@ size_t kda_prefill_workspace_bytes(int32_t num_seqs, int32_t H, int32_t d_k,
  *
  * If cu_seqlens violates its contract the kernels write nothing and set the
  * 32-bit word at byte offset 4 of the workspace to a nonzero value (it is
- * cleared to zero by every call that finds cu_seqlens valid).  This is a
- * device-side flag: reading it needs a synchronisation by the caller.
+ * cleared to zero by every call that finds cu_seqlens valid).  The 32-bit word
+ * at byte offset 8 gets bit 1 set if a wait inside the tensor-core kernel gave
+ * up after two seconds (which means a library fault; the kernel then stops
+ * early and its outputs are incomplete); the library never clears it, so a
+ * caller who wants to watch it zeroes it first.  Both are device-side flags:
+ * reading them needs a synchronisation by the caller.
+ *
+ * Paths: bf16 inputs with d_k = d_v = 128 run on the tensor cores (tcgen05,
+ * chunks of 64 tokens); every other supported shape, and every call made
+ * while the environment variable KDA_FORCE_SIMT is set, runs the fp32
+ * CUDA-core path (chunks of 16 tokens).  Both compute the same result up to
+ * rounding.
  */
 kda_status_t kda_prefill(const void *q, const void *k, const void *v,
                          const float *log_alpha, const float *beta,
