@@ -24,7 +24,7 @@ KDA_BF16, KDA_FP32, KDA_BF16_F32OUT = 0, 1, 2
 
 # Every symbol include/kda.h declares.
 EXPORTS = ("kda_prefill_workspace_bytes", "kda_prefill", "kda_decode_step",
-           "kda_status_string")
+           "kda_status_string", "kda_prefill_noalloc")
 
 
 class KdaError(RuntimeError):
@@ -57,6 +57,14 @@ def _declare(lib):
     return lib
 
 
+def _declare_noalloc(lib):
+    lib.kda_prefill_noalloc.restype = ctypes.c_int
+    lib.kda_prefill_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                        _i32, _i64, _i32, _i32, _i32, ctypes.c_int,
+                                        _vp, _vp, _vp]
+    return lib
+
+
 def lib():
     """The loaded libkda.so (ctypes handle).  Raises if it has not been built."""
     global _lib
@@ -66,7 +74,7 @@ def lib():
                 raise RuntimeError(
                     "libkda.so is not built (%s); run "
                     "`python -m gated_delta_rule_05_gb300._build`" % LIB_PATH)
-            _lib = _declare(ctypes.CDLL(LIB_PATH))
+            _lib = _declare_noalloc(_declare(ctypes.CDLL(LIB_PATH)))
         return _lib
 
 
@@ -191,3 +199,33 @@ def kda_decode_step(q, k, v, log_alpha, beta, S_inout, *, o=None, stream=None,
     if rc != KDA_OK:
         raise KdaError(rc, "kda_decode_step")
     return o
+
+
+def kda_prefill_noalloc(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, *,
+                        o, S_final=None, stream=None):
+    """kda_prefill without a workspace (C ABI: kda_prefill_noalloc), for
+    callers that cannot allocate device memory: the library uses a fixed
+    scratch array of its own (at most 4096 sequences).  ``o`` (and
+    ``S_final``, if wanted) must be given; this wrapper allocates nothing.
+    Returns (o, S_final)."""
+    torch = _torch()
+    T, H, dk = q.shape
+    dv = v.shape[2]
+    dt = _dtype_code(q, o.dtype)
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _check_cuda(name, t, q.dtype)
+    _check_cuda("log_alpha", log_alpha, torch.float32)
+    _check_cuda("beta", beta, torch.float32)
+    _check_cuda("S0", S0, torch.float32)
+    _check_cuda("cu_seqlens", cu_seqlens, torch.int32)
+    _check_cuda("o", o, o.dtype)
+    _check_cuda("S_final", S_final, torch.float32)
+    N = 1 if cu_seqlens is None else cu_seqlens.shape[0] - 1
+    with torch.cuda.device(q.device):
+        rc = lib().kda_prefill_noalloc(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(S0),
+            _ptr(cu_seqlens), N, T, H, dk, dv, dt, _ptr(o), _ptr(S_final),
+            _stream_handle(stream, q.device))
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_prefill_noalloc")
+    return o, S_final

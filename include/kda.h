@@ -133,6 +133,33 @@ kda_status_t kda_decode_step(const void *q, const void *k, const void *v,
                              int32_t d_v, kda_dtype_t dtype, void *o,
                              cudaStream_t stream);
 
+/* kda_prefill for callers that cannot allocate device memory.
+ *
+ * The pages have no counterpart to this entry point: it exists for callers
+ * that cannot call cudaMalloc, such as an inference engine that plans all of
+ * its device memory once at start-up and forbids allocation afterwards, or a
+ * plugin host that passes a library only the operation's inputs and outputs.
+ *
+ * Same arguments, layouts and results as kda_prefill, without the workspace:
+ * the work list lives in a fixed scratch array inside the library's device
+ * image (about 16 KiB, room for at most 4096 sequences; every GPU that loads
+ * the library keeps it until the process exits).  num_seqs above 4096
+ * returns KDA_ERR_WORKSPACE.  The first call on each device, with that device
+ * current, looks the array's device address up (cudaGetSymbolAddress, which
+ * may load the library's device code), so make that first call before any
+ * stream capture.  All calls on a device share the array: calls that may
+ * overlap on the GPU race on it and must be ordered by the caller.  Nothing
+ * is allocated and nothing in the array needs clearing between calls.
+ * KDA_ERR_CUDA is returned if the device or the array's address cannot be
+ * determined. */
+kda_status_t kda_prefill_noalloc(const void *q, const void *k, const void *v,
+                                 const float *log_alpha, const float *beta,
+                                 const float *S0, const int32_t *cu_seqlens,
+                                 int32_t num_seqs, int64_t total_tokens,
+                                 int32_t H, int32_t d_k, int32_t d_v,
+                                 kda_dtype_t dtype, void *o, float *S_final,
+                                 cudaStream_t stream);
+
 /* A static, human-readable name for a status code (never NULL). */
 const char *kda_status_string(kda_status_t status);
 
