@@ -40,10 +40,22 @@
 // CTA roles (320 threads, one CTA per (sequence, head)):
 //   warp 0      TMA: q, k, g tiles (64 x 128) and the v tile, beta by plain loads
 //   warp 1      one thread issues every tcgen05.mma and commit
-//   warps 2..5  producer: thread c = key channel c; gate prep, Gram readout,
-//               UT solve, W readout
-//   warps 6..9  consumer: thread v = value column v (TMEM lane v); state
-//               decay + bf16 copy, U readout, O readout, S_final
+//   warps 2..9  the compute group (256 threads) runs every CUDA-core phase of a
+//               chunk together: gate prep, state decay, Gram readout, the UT
+//               solve's diagonal blocks, and every TMEM readout.  The chunk's steps form one
+//               dependency chain, so the group moves through it as a whole;
+//               the state decay overlaps the Gram product on the tensor cores.
+// UT solve.  With D the inverse of the 16 x 16 diagonal blocks of L = I + A
+// (forward substitution on CUDA cores) and N = D A_off (A_off = the blocks
+// below the diagonal), N is nilpotent of order 4, so
+//     (I + A)^{-1} = (I + N)^{-1} D = (I - N)(I + N^2) D,
+// and T = (I + A)^{-1} Diag(b) = (I - N)(I + N^2) D'  with D' = D Diag(b).
+// The four 64 x 64 products N = D A_off, N^2, Y = D' + N^2 D' and
+// T = Y - N Y run on the tensor cores with fp16 operands (the small
+// triangular inverse becomes dense products, as the UT transform intends).
+// They use tensor memory and shared memory that are idle at that point of
+// the chunk; the MMA has M = 128 and only rows 0..63 are read back.
+//
 // Every wait is bounded in time; a timeout sets a flag in the workspace,
 // drains the CTA and frees its tensor memory.
 #include <cudaTypedefs.h>
@@ -61,6 +73,8 @@ using namespace sm100;
 constexpr int kC = 64;
 constexpr int kD = 128;
 constexpr int kThreads = 320;
+constexpr int kGroup = 256;            // compute group: warps 2..9
+constexpr int kGroupBar = 1;           // its named barrier
 constexpr float kLog2e = 1.4426950408889634f;
 // Largest decay span (in log2 units) handled in one pass: both Gram factors
 // stay below 2^125.
@@ -79,35 +93,55 @@ constexpr uint32_t OFF_WT = 139264;    // -W^T    [ch][r] fp16
 constexpr uint32_t OFF_QG = 155648;    // (e^G Q)^T [ch][r] fp16
 constexpr uint32_t OFF_P = 172032;     // P       [r][i] fp16
 constexpr uint32_t OFF_KT = 180224;    // Ktil^T  [ch][i] fp16
-constexpr uint32_t OFF_A32 = 196608;   // A / X   fp32 [64][65]; before the Gram readout:
-constexpr uint32_t OFF_BDLO = OFF_A32; //   Gram B lo part [ch][Kc lo] bf16
-constexpr uint32_t OFF_T16 = 214016;   // T       [r][i] fp16 (V product)
-constexpr uint32_t OFF_Y = 222208;     // solve scratch, fp32 3 x 256
+constexpr uint32_t OFF_A32 = 196608;   // A, then X = (I+A)^-1: fp32 [64][68]; before the
+constexpr uint32_t OFF_BDLO = OFF_A32; //   Gram readout: Gram B lo part [ch][Kc lo] bf16
+constexpr uint32_t OFF_T16 = 214016;   // T       [r][i] fp16 (V product); during gate prep:
+constexpr uint32_t OFF_STAT = OFF_T16; //   per row-quarter decay stats, fp32 [3][4][128]
+constexpr uint32_t OFF_Y = 222208;     // (spare)
+// Solve tiles, all fp16, in regions idle during the solve (the g tile's and
+// the Gram B tile's space; the next q/k/g load waits for them):
+constexpr uint32_t OFF_DM = OFF_G;            // D  as MN-major A [k][r]
+constexpr uint32_t OFF_AO = OFF_G + 8192;     // A_off as MN-major B [k][c]
+constexpr uint32_t OFF_NB = OFF_G + 16384;    // N  as MN-major B [m][c]
+constexpr uint32_t OFF_DPK = OFF_G + 24576;   // D' as K-major B [c][m] (column c of D')
+constexpr uint32_t OFF_YB = OFF_BD;           // Y  as MN-major B [m][c]
+// O tile staging for the TMA store, [64 tok][128 v] bf16 plain rows (the A / X
+// region, idle from the end of the solve until the next chunk's Gram operands):
+constexpr uint32_t OFF_OST = OFF_A32;
 constexpr uint32_t OFF_GL = 225280;    // e^{G_last} per channel
 constexpr uint32_t OFF_R = 225792;     // 2^R per channel
 constexpr uint32_t OFF_BIN = 226304;   // beta of the loaded chunk
 constexpr uint32_t OFF_BST = 226560;   // beta of the current pass (masked)
 constexpr uint32_t OFF_DESC = 226816;  // 2 step descriptors
-constexpr uint32_t OFF_BAR = 226880;   // mbarriers
-constexpr uint32_t OFF_MISC = 227008;  // tmem base, flags
+constexpr uint32_t OFF_BAR = 226880;   // mbarriers (20 x 8 B)
+constexpr uint32_t OFF_MISC = 227040;  // tmem base, flags
 constexpr uint32_t kSmemUsed = 227072;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;   // + alignment slack
-constexpr int LDA = 65;
+constexpr int LDA = 68;                // row stride (floats) of A / X: 16-byte aligned rows
 
 enum Bar {
     B_QKG_FULL = 0, B_QKG_EMPTY, B_V_FULL, B_V_EMPTY, B_OPS, B_MMA_G, B_T, B_MMA_W,
-    B_W, B_S, B_MMA_C, B_U, B_MMA_OS, B_O_FREE, kNumBars
+    B_CV, B_MMA_C, B_U, B_MMA_OS,
+    B_S1, B_R1, B_S2, B_R2, B_S3, B_R3, B_S4, B_R4,   // UT solve rounds
+    kNumBars
 };
 
-// TMEM columns (512 allocated).
-constexpr uint32_t TM_S = 0;      // S^T fp32 [v][ch]          128 cols
-constexpr uint32_t TM_SB = 128;   // S^T fp16 A operand         64 cols
-constexpr uint32_t TM_C = 192;    // U^T fp32 [v][r]            64 cols
-constexpr uint32_t TM_UB = 256;   // U^T fp16 A operand         32 cols
-constexpr uint32_t TM_O = 288;    // O^T fp32 [v][r]            64 cols
-constexpr uint32_t TM_G = 352;    // Gram [Kr rows; Qr rows][i]  64 cols
-constexpr uint32_t TM_W = 416;    // W^T (unscaled) [ch][r]      64 cols
+// TMEM columns (512 allocated).  C|O and O|S are adjacent so that one MMA
+// can write both of a pair.
+constexpr uint32_t TM_G = 0;      // Gram [Kr rows; Qr rows] x [Kc hi | Kc lo]   128 cols
+constexpr uint32_t TM_W = 0;      // W^T (unscaled) [ch][r], after the solve      64 cols
+constexpr uint32_t TM_SB = 128;   // S^T fp16 A operand                           64 cols
+constexpr uint32_t TM_C = 192;    // U^T fp32 [v][r]                              64 cols
+constexpr uint32_t TM_O = 256;    // O^T fp32 [v][r]                              64 cols
+constexpr uint32_t TM_S = 320;    // S^T fp32 [v][ch]                            128 cols
+constexpr uint32_t TM_UB = 448;   // U^T fp16 A operand                           32 cols
 constexpr uint32_t kTmemCols = 512;
+// During the UT solve (rows 0..63 used), in columns otherwise idle then:
+constexpr uint32_t TM_N = 0;      // N = D A_off, fp32
+constexpr uint32_t TM_N2A = 64;   // N^2 as fp16 A operand
+constexpr uint32_t TM_IA = 96;    // identity rows as fp16 A operand
+constexpr uint32_t TM_NA = TM_UB; // N as fp16 A operand
+constexpr uint32_t TM_N2 = TM_C;  // N^2, fp32; then Y, then T
 
 struct StepDesc {
     int32_t t0, len, lo, hi, first_pass, last_pass, last_step, chunk;
@@ -116,7 +150,7 @@ struct StepDesc {
 struct Misc {
     uint32_t tmem_base;
     int32_t abort;
-    int32_t wide;      // producer vote: this chunk needs two passes
+    int32_t wide;      // vote: this chunk needs two passes
     int32_t pad;
 };
 
@@ -126,10 +160,15 @@ __device__ __forceinline__ void st_chunk(uint8_t* tile, int row, int chunk, uint
     *reinterpret_cast<uint4*>(tile + off) = val;
 }
 
-__device__ __forceinline__ float bf2f(const uint8_t* p)
+__device__ __forceinline__ float ex2(float x)
 {
-    return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(p));
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
+
+__device__ __forceinline__ float lo_bf16(uint32_t x) { return __uint_as_float(x << 16); }
+__device__ __forceinline__ float hi_bf16(uint32_t x) { return __uint_as_float(x & 0xFFFF0000u); }
 
 __device__ __forceinline__ void out_store(float* p, float x) { *p = x; }
 __device__ __forceinline__ void out_store(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
@@ -151,80 +190,43 @@ __device__ __forceinline__ bool wait_bar(const Ctx& X, int b, uint32_t phase)
     return false;
 }
 
-// Producer / consumer warpgroups: wait, then agree on abort at a named barrier
-// (every thread passes the barrier, so no thread is left waiting on it).
-__device__ __forceinline__ bool wg_wait(const Ctx& X, int b, uint32_t phase, int bar_id)
+// The compute group waits, then agrees on abort at its named barrier (every
+// thread passes the barrier, so no thread is left waiting on it).
+__device__ __forceinline__ bool group_wait(const Ctx& X, int b, uint32_t phase)
 {
     wait_bar(X, b, phase);
-    named_bar_sync(bar_id, 128);
+    named_bar_sync(kGroupBar, kGroup);
     return *reinterpret_cast<volatile int32_t*>(&X.misc->abort) == 0;
 }
 
-// ------------------------------------------------------------ UT solve
-// On entry sA holds the strictly lower triangular A (fp32, stride 65; zero on
-// and above the diagonal).  On exit it holds X = (I + A)^{-1} (unit lower
-// triangular): the strictly lower parts of the 16 x 16 diagonal blocks in
-// place, and each off-diagonal block X_ij (i > j) at the mirrored position,
-// so that X[r][c] for r > c in different blocks is sA[c*65 + r].  The block
-// recursion X_ij = -X_ii sum_{j<=k<i} A_ik X_kj turns the inverse into small
-// dense products; the 16 x 16 diagonal blocks use forward substitution.
-__device__ __forceinline__ float x_at(const float* sA, int r, int c)
+__device__ __forceinline__ void group_sync() { named_bar_sync(kGroupBar, kGroup); }
+
+// 16 x 16 unit-lower diagonal block inverse, column j (j < 16) of block b by
+// forward substitution; x[r] for r < j is 0 and x[j] is 1.
+__device__ __forceinline__ void diag_block_column(const float* sA, int b, int j, float (&x)[16])
 {
-    if (r == c) return 1.f;
-    if (r < c) return 0.f;
-    return ((r >> 4) == (c >> 4)) ? sA[r * LDA + c] : sA[c * LDA + r];
+    const float* L = sA + (b * 16) * LDA + b * 16;
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+        float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+        for (int i = 0; i < r; ++i) {
+            if (i & 1) a1 = fmaf(L[r * LDA + i], x[i], a1);
+            else a0 = fmaf(L[r * LDA + i], x[i], a0);
+        }
+        x[r] = (r == j) ? 1.f : ((r < j) ? 0.f : -(a0 + a1));
+    }
 }
 
-__device__ void ut_solve(float* sA, float* sY, int tid, int bar_id)
+// Reads 32 fp32 columns of a TMEM row, converts them to 16 packed fp16 pairs.
+__device__ __forceinline__ void tmem_row_f16(uint32_t taddr, uint32_t (&out)[16])
 {
-    {   // diagonal blocks: warp b, lane j < 16 computes column j
-        const int b = tid >> 5, j = tid & 31;
-        float x[16];
-        const float* L = sA + (b * 16) * LDA + b * 16;
+    uint32_t d[32];
+    tmem_ld32(taddr, d);
+    tmem_ld_wait();
 #pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-            for (int i = 0; i < r; ++i) {
-                if (i & 1) a1 = fmaf(L[r * LDA + i], x[i], a1);
-                else a0 = fmaf(L[r * LDA + i], x[i], a0);
-            }
-            x[r] = (r == j) ? 1.f : ((r < j) ? 0.f : -(a0 + a1));
-        }
-        __syncwarp();
-        if (j < 16) {
-#pragma unroll
-            for (int r = 0; r < 16; ++r)
-                if (r > j) sA[(b * 16 + r) * LDA + b * 16 + j] = x[r];
-        }
-    }
-    named_bar_sync(bar_id, 128);
-    // off-diagonal blocks, by distance d from the diagonal
-    for (int d = 1; d < 4; ++d) {
-        const int nblk = 4 - d;
-        for (int e = tid; e < nblk * 256; e += 128) {
-            const int blk = e >> 8, r = (e >> 4) & 15, c = e & 15;
-            const int j = blk, i = blk + d;
-            float y = 0.f;
-            for (int kb = j; kb < i; ++kb) {
-                const float* Arow = sA + (i * 16 + r) * LDA + kb * 16;
-#pragma unroll
-                for (int m = 0; m < 16; ++m)
-                    y = fmaf(Arow[m], x_at(sA, kb * 16 + m, j * 16 + c), y);
-            }
-            sY[e] = y;
-        }
-        named_bar_sync(bar_id, 128);
-        for (int e = tid; e < nblk * 256; e += 128) {
-            const int blk = e >> 8, r = (e >> 4) & 15, c = e & 15;
-            const int j = blk, i = blk + d;
-            float x = sY[e];
-            const float* Xrow = sA + (i * 16 + r) * LDA + i * 16;
-            for (int m = 0; m < r; ++m) x = fmaf(Xrow[m], sY[(blk << 8) + (m << 4) + c], x);
-            sA[(j * 16 + c) * LDA + i * 16 + r] = -x;   // mirrored storage
-        }
-        named_bar_sync(bar_id, 128);
-    }
+    for (int i = 0; i < 16; ++i)
+        out[i] = pack_f16x2(__uint_as_float(d[2 * i]), __uint_as_float(d[2 * i + 1]));
 }
 
 // ------------------------------------------------------------- the kernel
@@ -232,6 +234,7 @@ template <typename TO>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUtensorMap tm_v,
+                  const __grid_constant__ CUtensorMap tm_o,
                   const float* __restrict__ beta, const float* S0,
                   const int32_t* __restrict__ cu, int32_t* ws, long long total_tokens, int H,
                   TO* __restrict__ o, float* S_final)
@@ -243,7 +246,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     X.bar = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
     X.desc = reinterpret_cast<StepDesc*>(sm + OFF_DESC);
     X.misc = reinterpret_cast<Misc*>(sm + OFF_MISC);
-    X.ws_err = ws + 2;
+    X.ws_err = ws + kWsTimeoutWord;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int rank = blockIdx.x / H, h = blockIdx.x % H;
@@ -281,6 +284,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_g);
             tma_prefetch_desc(&tm_v);
+            tma_prefetch_desc(&tm_o);
         }
         float* sBin = reinterpret_cast<float*>(sm + OFF_BIN);
         int issued_qkg = 0, issued_v = 0;
@@ -323,128 +327,235 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA
         if (lane == 0 && nch > 0) {
-            const uint32_t id_g = make_idesc_bf16(128, 64, true, true);     // Gram
+            const uint32_t id_g = make_idesc_bf16(128, 128, true, true);    // Gram
             const uint32_t id_w = make_idesc_bf16(128, 64, false, false);   // W
             const uint32_t id_cv = make_idesc_f16(128, 64, true, false);    // V^T T^T
             const uint32_t id_mn = make_idesc_f16(128, 64, false, true);    // S^T x MN-major B
             const uint32_t id_k64 = make_idesc_f16(128, 64, false, false);  // U^T P^T
-            const uint32_t id_s = make_idesc_f16(128, 128, false, false);   // U^T Ktil
-            const uint32_t a_ad = smem_u32(sm + OFF_AD), a_bd = smem_u32(sm + OFF_BD);
-            const uint32_t a_adlo = smem_u32(sm + OFF_ADLO), a_bdlo = smem_u32(sm + OFF_BDLO);
-            const uint32_t a_t = smem_u32(sm + OFF_T), a_t16 = smem_u32(sm + OFF_T16);
-            const uint32_t a_v = smem_u32(sm + OFF_V);
-            const uint32_t a_wt = smem_u32(sm + OFF_WT), a_qg = smem_u32(sm + OFF_QG);
-            const uint32_t a_p = smem_u32(sm + OFF_P), a_kt = smem_u32(sm + OFF_KT);
+            const uint32_t id_os = make_idesc_f16(128, 192, false, false);  // U^T [P | Ktil]^T
+            const uint32_t id_mn128 = make_idesc_f16(128, 128, false, true); // S^T [-W^T | (e^G Q)^T]
+            // Base descriptors; a K step advances the start address field
+            // (16-byte units) by 128 for MN-major tiles, by 2 for K-major ones.
+            const uint64_t dAD = make_sdesc(smem_u32(sm + OFF_AD), 16384, 1024, kSwizzle128B);
+            const uint64_t dADLO = make_sdesc(smem_u32(sm + OFF_ADLO), 16384, 1024, kSwizzle128B);
+            const uint64_t dBDHL = make_sdesc(smem_u32(sm + OFF_BD), OFF_BDLO - OFF_BD, 1024, kSwizzle128B);
+            const uint64_t dADK = make_sdesc(smem_u32(sm + OFF_AD), 16, 1024, kSwizzle128B);
+            const uint64_t dT = make_sdesc(smem_u32(sm + OFF_T), 16, 1024, kSwizzle128B);
+            const uint64_t dT16 = make_sdesc(smem_u32(sm + OFF_T16), 16, 1024, kSwizzle128B);
+            const uint64_t dV = make_sdesc(smem_u32(sm + OFF_V), 8192, 1024, kSwizzle128B);
+            const uint64_t dWQ = make_sdesc(smem_u32(sm + OFF_WT), OFF_QG - OFF_WT, 1024, kSwizzle128B);
+            const uint64_t dPK = make_sdesc(smem_u32(sm + OFF_P), 16, 1024, kSwizzle128B);
+            // D as the A operand of N = D A_off: M = 128 with the second 64-row
+            // block pointed at the next tile (finite data; its rows are unused).
+            const uint64_t dDM = make_sdesc(smem_u32(sm + OFF_DM), 8192, 1024, kSwizzle128B);
+            const uint64_t dAO = make_sdesc(smem_u32(sm + OFF_AO), 8192, 1024, kSwizzle128B);
+            const uint64_t dNB = make_sdesc(smem_u32(sm + OFF_NB), 8192, 1024, kSwizzle128B);
+            const uint64_t dDPK = make_sdesc(smem_u32(sm + OFF_DPK), 16, 1024, kSwizzle128B);
+            const uint64_t dYB = make_sdesc(smem_u32(sm + OFF_YB), 8192, 1024, kSwizzle128B);
+            const uint32_t id_r1 = make_idesc_f16(128, 64, true, true);
+            const uint32_t id_mn_neg = make_idesc_f16(128, 64, false, true, true);
             for (int step = 0;; ++step) {
                 if (!wait_bar(X, B_OPS, step)) break;
                 tc_fence_after();
                 const StepDesc d = X.desc[step & 1];
-                // Gram: [Kr; Qr] (MN-major A) x Kc (MN-major B), K = 128 channels,
-                // as hi.hi + lo.hi + hi.lo.
+                // Gram: [Kr; Qr] (MN-major A) x [Kc hi | Kc lo] (MN-major B, N = 128),
+                // K = 128 channels, hi and lo A parts: the readout adds the halves.
+#pragma unroll
                 for (int s = 0; s < 8; ++s)
-                    mma_ss(tmem + TM_G, make_sdesc(a_ad + s * 2048, 16384, 1024, kSwizzle128B),
-                           make_sdesc(a_bd + s * 2048, 8192, 1024, kSwizzle128B), id_g, s > 0);
+                    mma_ss(tmem + TM_G, dAD + 128 * s, dBDHL + 128 * s, id_g, s > 0);
+#pragma unroll
                 for (int s = 0; s < 8; ++s)
-                    mma_ss(tmem + TM_G, make_sdesc(a_adlo + s * 2048, 16384, 1024, kSwizzle128B),
-                           make_sdesc(a_bd + s * 2048, 8192, 1024, kSwizzle128B), id_g, 1);
-                for (int s = 0; s < 8; ++s)
-                    mma_ss(tmem + TM_G, make_sdesc(a_ad + s * 2048, 16384, 1024, kSwizzle128B),
-                           make_sdesc(a_bdlo + s * 2048, 8192, 1024, kSwizzle128B), id_g, 1);
+                    mma_ss(tmem + TM_G, dADLO + 128 * s, dBDHL + 128 * s, id_g, 1);
                 mma_commit(&X.bar[B_MMA_G]);
+                // UT solve: N = D A_off ; N^2 = N N ; Y = I D' + N^2 D' ; T = Y - N Y.
+                if (!wait_bar(X, B_S1, step)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int s = 0; s < 4; ++s)
+                    mma_ss(tmem + TM_N, dDM + 128 * s, dAO + 128 * s, id_r1, s > 0);
+                mma_commit(&X.bar[B_R1]);
+                if (!wait_bar(X, B_S2, step)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int s = 0; s < 4; ++s)
+                    mma_ts(tmem + TM_N2, tmem + TM_NA + 8 * s, dNB + 128 * s, id_mn, s > 0);
+                mma_commit(&X.bar[B_R2]);
+                if (!wait_bar(X, B_S3, step)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int s = 0; s < 4; ++s)
+                    mma_ts(tmem + TM_N2, tmem + TM_IA + 8 * s, dDPK + 2 * s, id_k64, s > 0);
+#pragma unroll
+                for (int s = 0; s < 4; ++s)
+                    mma_ts(tmem + TM_N2, tmem + TM_N2A + 8 * s, dDPK + 2 * s, id_k64, 1);
+                mma_commit(&X.bar[B_R3]);
+                if (!wait_bar(X, B_S4, step)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int s = 0; s < 4; ++s)
+                    mma_ts(tmem + TM_N2, tmem + TM_NA + 8 * s, dYB + 128 * s, id_mn_neg, 1);
+                mma_commit(&X.bar[B_R4]);
                 if (!wait_bar(X, B_T, step)) break;
                 tc_fence_after();
                 // W^T (unscaled) = Kr^T T^T: A = Kr hi as K-major [ch][tok], B = T [r][i].
-                for (int s = 0; s < 4; ++s)
-                    mma_ss(tmem + TM_W, make_sdesc(a_ad + s * 32, 16, 1024, kSwizzle128B),
-                           make_sdesc(a_t + s * 32, 16, 1024, kSwizzle128B), id_w, s > 0);
+#pragma unroll
+                for (int s = 0; s < 4; ++s) mma_ss(tmem + TM_W, dADK + 2 * s, dT + 2 * s, id_w, s > 0);
                 mma_commit(&X.bar[B_MMA_W]);
-                if (!wait_bar(X, B_W, step)) break;
-                if (!wait_bar(X, B_S, step)) break;     // also: v tile converted to fp16
-                if (step > 0 && !wait_bar(X, B_O_FREE, step - 1)) break;
+                if (!wait_bar(X, B_CV, step)) break;   // -W^T, S^T copy, v tile ready
                 tc_fence_after();
-                // U^T = V^T T^T - S^T W^T
+                // [U^T | O^T] = S^T [-W^T | (e^G Q)^T] ;  U^T += V^T T^T
+                // (the U^T P^T term of O^T follows once U^T is ready)
+#pragma unroll
+                for (int s = 0; s < 8; ++s)
+                    mma_ts(tmem + TM_C, tmem + TM_SB + s * 8, dWQ + 128 * s, id_mn128, s > 0);
+#pragma unroll
                 for (int s = 0; s < 4; ++s)
-                    mma_ss(tmem + TM_C, make_sdesc(a_v + s * 2048, 8192, 1024, kSwizzle128B),
-                           make_sdesc(a_t16 + s * 32, 16, 1024, kSwizzle128B), id_cv, s > 0);
-                for (int s = 0; s < 8; ++s)
-                    mma_ts(tmem + TM_C, tmem + TM_SB + s * 8,
-                           make_sdesc(a_wt + s * 2048, 8192, 1024, kSwizzle128B), id_mn, 1);
-                // O^T = S^T (e^G Q)^T  (the U^T P^T term follows once U^T is ready)
-                for (int s = 0; s < 8; ++s)
-                    mma_ts(tmem + TM_O, tmem + TM_SB + s * 8,
-                           make_sdesc(a_qg + s * 2048, 8192, 1024, kSwizzle128B), id_mn, s > 0);
+                    mma_ss(tmem + TM_C, dV + 128 * s, dT16 + 2 * s, id_cv, 1);
                 mma_commit(&X.bar[B_MMA_C]);
                 if (d.last_pass) mma_commit(&X.bar[B_V_EMPTY]);
                 if (!wait_bar(X, B_U, step)) break;
                 tc_fence_after();
-                // O^T += U^T P^T ;  S^T += U^T Ktil
+                // [O^T | S^T] += U^T [P | Ktil^T]^T   (N = 64 + 128)
+#pragma unroll
                 for (int s = 0; s < 4; ++s)
-                    mma_ts(tmem + TM_O, tmem + TM_UB + s * 8,
-                           make_sdesc(a_p + s * 32, 16, 1024, kSwizzle128B), id_k64, 1);
-                for (int s = 0; s < 4; ++s)
-                    mma_ts(tmem + TM_S, tmem + TM_UB + s * 8,
-                           make_sdesc(a_kt + s * 32, 16, 1024, kSwizzle128B), id_s, 1);
+                    mma_ts(tmem + TM_O, tmem + TM_UB + s * 8, dPK + 2 * s, id_os, 1);
                 mma_commit(&X.bar[B_MMA_OS]);
                 if (d.last_step) break;
             }
         }
-    } else if (warp < 6) {
-        // ------------------------------------------------------- producer
-        const int c = ((warp & 3) << 5) | lane;          // key channel == TMEM lane
-        const int ptid = tid - 64;                        // 0..127 within the group
+    } else {
+        // -------------------------------------------------- compute group
+        const int ct = tid - 64;                           // 0..255
+        const int half = ct >> 7;                          // which half of a TMEM row
+        const int L = ((warp & 3) << 5) | lane;            // this thread's TMEM lane
         const uint32_t lane_base = (uint32_t)((warp & 3) << 5) << 16;
+        // gate-prep mapping: channels 2cp, 2cp+1; rows 16rq .. 16rq+15
+        const int cp = ct & 63, rq = ct >> 6;
         const uint8_t* sQ = sm + OFF_Q;
         const uint8_t* sK = sm + OFF_K;
         const float* sG = reinterpret_cast<const float*>(sm + OFF_G);
         const float* sBin = reinterpret_cast<const float*>(sm + OFF_BIN);
+        float* sStat = reinterpret_cast<float*>(sm + OFF_STAT);   // [3][4][128]
         float* sBst = reinterpret_cast<float*>(sm + OFF_BST);
         float* sGl = reinterpret_cast<float*>(sm + OFF_GL);
         float* sR = reinterpret_cast<float*>(sm + OFF_R);
         float* sA = reinterpret_cast<float*>(sm + OFF_A32);
-        float* sY = reinterpret_cast<float*>(sm + OFF_Y);
-        int step = 0;
+
+        // S^T <- S0^T (row v of S^T is column v of S0); this thread: 64 channels.
+#pragma unroll
+        for (int jb = 0; jb < 2; ++jb) {
+            uint32_t r[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const int c = 64 * half + 32 * jb + i;
+                r[i] = __float_as_uint(S0 ? S0[sbase + (long long)c * kD + L] : 0.f);
+            }
+            tmem_st32(tmem + lane_base + TM_S + 64 * half + 32 * jb, r);
+        }
+        tmem_st_wait();
+
+        int step = 0, chunk_v = 0;
         bool alive = true;
         for (int ch = 0; ch < nch && alive; ++ch) {
             const long long t0 = bos + (long long)ch * kC;
             const int len = (eos - t0 < kC) ? (int)(eos - t0) : kC;
-            if (!wg_wait(X, B_QKG_FULL, ch, 1)) break;
-            // Running log2-decay over the chunk (kept in registers: the g tile's
-            // smem is reused for the Gram lo parts), and its span.
-            float Gf[kC];
-            float G = 0.f, gmax = 0.f, gmin = 0.f;
+            if (!group_wait(X, B_QKG_FULL, ch)) break;
+            // ---- decay scan of this thread's 16 rows x 2 channels (log2 units,
+            // relative to the start of its row quarter); kept in registers.
+            float2 Gq[16];
+            {
+                float2 G = make_float2(0.f, 0.f), mx = G, mn = G;
 #pragma unroll
-            for (int r = 0; r < kC; ++r) {
-                G += (r < len) ? sG[r * kD + c] * kLog2e : 0.f;
-                Gf[r] = G;
-                gmax = fmaxf(gmax, G);
-                gmin = fminf(gmin, G);
+                for (int rr = 0; rr < 16; ++rr) {
+                    const int r = 16 * rq + rr;
+                    const float2 g = (r < len) ? *reinterpret_cast<const float2*>(sG + r * kD + 2 * cp)
+                                               : make_float2(0.f, 0.f);
+                    G.x = fmaf(g.x, kLog2e, G.x);
+                    G.y = fmaf(g.y, kLog2e, G.y);
+                    Gq[rr] = G;
+                    mx.x = fmaxf(mx.x, G.x); mx.y = fmaxf(mx.y, G.y);
+                    mn.x = fminf(mn.x, G.x); mn.y = fminf(mn.y, G.y);
+                }
+                *reinterpret_cast<float2*>(sStat + (0 * 4 + rq) * kD + 2 * cp) = G;
+                *reinterpret_cast<float2*>(sStat + (1 * 4 + rq) * kD + 2 * cp) = mx;
+                *reinterpret_cast<float2*>(sStat + (2 * 4 + rq) * kD + 2 * cp) = mn;
             }
-            if (gmax - gmin > kSpanMax) atomicExch(&X.misc->wide, 1);
-            named_bar_sync(1, 128);
-            const int npass = X.misc->wide ? 2 : 1;
-            named_bar_sync(1, 128);                       // all have read the vote (and sG)
-            if (ptid == 0) X.misc->wide = 0;
+            group_sync();
+            // Per channel: the four per-quarter (total, max, min) triples, read once.
+            // They give the span over the whole chunk (the two-pass vote) and, for
+            // either pass layout, R, 2^R, 2^{G_last - R}, e^{G_last} and the decay
+            // at the start of this thread's row quarter.
+            float st[3][4][2];
+#pragma unroll
+            for (int k = 0; k < 3; ++k)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float2 x = *reinterpret_cast<const float2*>(sStat + (k * 4 + q) * kD + 2 * cp);
+                    st[k][q][0] = x.x;
+                    st[k][q][1] = x.y;
+                }
+            auto range = [&](int u, int qa, int qb, float& pmax, float& pmin, float& tot) {
+                float off = 0.f;
+                pmax = 0.f;
+                pmin = 0.f;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    if (q < qa || q > qb) continue;
+                    pmax = fmaxf(pmax, off + st[1][q][u]);
+                    pmin = fminf(pmin, off + st[2][q][u]);
+                    off += st[0][q][u];
+                }
+                tot = off;
+            };
+            bool wide_me = false;
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                float a, b, t;
+                range(u, 0, 3, a, b, t);
+                wide_me = wide_me || (a - b > kSpanMax);
+            }
+            const int npass = named_bar_red_or(kGroupBar, kGroup, wide_me) ? 2 : 1;
+            float R[2][2], pR[2][2], pL[2][2], gl[2][2], base[2][2];
+#pragma unroll
+            for (int p = 0; p < 2; ++p) {
+                const int qa = (npass == 1) ? 0 : 2 * p, qb = (npass == 1) ? 3 : 2 * p + 1;
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    float pmax, pmin, tot;
+                    range(u, qa, qb, pmax, pmin, tot);
+                    R[p][u] = 0.5f * (pmax + pmin);
+                    pR[p][u] = ex2(R[p][u]);
+                    pL[p][u] = ex2(tot - R[p][u]);
+                    gl[p][u] = ex2(tot);
+                    float b = 0.f;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        if (q >= qa && q < rq) b += st[0][q][u];
+                    base[p][u] = b;
+                }
+            }
             for (int p = 0; p < npass; ++p) {
                 const int lo = (npass == 1) ? 0 : (p == 0 ? 0 : 32);
                 const int hi = (npass == 1) ? len : (p == 0 ? min(32, len) : len);
-                // log2-decay of this pass, relative to the row before its first row
-                const float base = (lo > 0) ? Gf[31] : 0.f;    // lo is 0 or 32
-                float Glast = 0.f;
-                gmax = 0.f;
-                gmin = 0.f;
+                // this pass's parameters (selected, so the arrays stay in registers)
+                float Rc[2], pRc[2], pLc[2], glc[2], basec[2];
 #pragma unroll
-                for (int r = 0; r < kC; ++r) {
-                    if (r >= lo && r < hi) {
-                        Glast = Gf[r] - base;
-                        gmax = fmaxf(gmax, Glast);
-                        gmin = fminf(gmin, Glast);
+                for (int u = 0; u < 2; ++u) {
+                    Rc[u] = p ? R[1][u] : R[0][u];
+                    pRc[u] = p ? pR[1][u] : pR[0][u];
+                    pLc[u] = p ? pL[1][u] : pL[0][u];
+                    glc[u] = p ? gl[1][u] : gl[0][u];
+                    basec[u] = p ? base[1][u] : base[0][u];
+                }
+                if (rq == 0) {
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        sGl[2 * cp + u] = glc[u];
+                        sR[2 * cp + u] = pRc[u];
                     }
                 }
-                const float R = 0.5f * (gmax + gmin);
-                const float pR = exp2f(R);
-                const float pL = exp2f(Glast - R);
-                if (step > 0 && !wg_wait(X, B_MMA_OS, step - 1, 1)) { alive = false; break; }
-                if (ptid == 0) {
+                if (ct < kC) sBst[ct] = (ct >= lo && ct < hi) ? sBin[ct] : 0.f;
+                if (ct == 0) {
                     StepDesc d;
                     d.t0 = (int32_t)t0;
                     d.len = len;
@@ -456,258 +567,374 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     d.chunk = ch;
                     X.desc[step & 1] = d;
                 }
-                // Gram operands as bf16 hi/lo pairs; e^G Q and Ktil as fp16.
+                // The previous chunk's O store has read its staging area (the
+                // Gram B lo part goes there), and everyone has read the decay
+                // stats before the lo parts overwrite the g tile.
+                if (ct == 0) bulk_wait_group_read0();
+                group_sync();
+                // ---- Gram operands (bf16 hi/lo), e^G Q and Ktil (fp16); this
+                // thread writes 2 channels x 2 chunks of 8 rows of each.
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    uint32_t krh[4], krl[4], qrh[4], qrl[4], kch[4], kcl[4], gq[4], kt[4];
+                for (int jj = 0; jj < 2; ++jj) {
+                    uint32_t kp[8], qp[8];             // bf16 pairs (channels 2cp, 2cp+1)
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        float vk[2], vq[2], vc[2], vg[2], vt[2];
-#pragma unroll
-                        for (int u = 0; u < 2; ++u) {
-                            const int r = j * 8 + e * 2 + u;
-                            const bool act = (r >= lo && r < hi);
-                            const float kk = act ? bf2f(sK + r * 256 + c * 2) : 0.f;
-                            const float qq = act ? bf2f(sQ + r * 256 + c * 2) : 0.f;
-                            const float gv = Gf[r] - base;    // pass-local log2-decay
-                            const float e1 = act ? exp2f(gv - R) : 0.f;
-                            const float e2 = act ? exp2f(R - gv) : 0.f;
-                            vk[u] = kk * e1;
-                            vq[u] = qq * e1;
-                            vc[u] = kk * e2;
-                            vg[u] = vq[u] * pR;
-                            vt[u] = vc[u] * pL;
-                        }
-                        krh[e] = pack_bf16x2(vk[0], vk[1]);
-                        qrh[e] = pack_bf16x2(vq[0], vq[1]);
-                        kch[e] = pack_bf16x2(vc[0], vc[1]);
-                        krl[e] = pack_bf16x2(vk[0] - __uint_as_float(krh[e] << 16),
-                                             vk[1] - __uint_as_float(krh[e] & 0xFFFF0000u));
-                        qrl[e] = pack_bf16x2(vq[0] - __uint_as_float(qrh[e] << 16),
-                                             vq[1] - __uint_as_float(qrh[e] & 0xFFFF0000u));
-                        kcl[e] = pack_bf16x2(vc[0] - __uint_as_float(kch[e] << 16),
-                                             vc[1] - __uint_as_float(kch[e] & 0xFFFF0000u));
-                        gq[e] = pack_f16x2(vg[0], vg[1]);
-                        kt[e] = pack_f16x2(vt[0], vt[1]);
+                    for (int w8 = 0; w8 < 8; ++w8) {
+                        const int r = 16 * rq + 8 * jj + w8;
+                        kp[w8] = *reinterpret_cast<const uint32_t*>(sK + r * 256 + 4 * cp);
+                        qp[w8] = *reinterpret_cast<const uint32_t*>(sQ + r * 256 + 4 * cp);
                     }
-                    st_chunk(sm + OFF_AD, c, j, make_uint4(krh[0], krh[1], krh[2], krh[3]));
-                    st_chunk(sm + OFF_AD + 16384, c, j, make_uint4(qrh[0], qrh[1], qrh[2], qrh[3]));
-                    st_chunk(sm + OFF_ADLO, c, j, make_uint4(krl[0], krl[1], krl[2], krl[3]));
-                    st_chunk(sm + OFF_ADLO + 16384, c, j, make_uint4(qrl[0], qrl[1], qrl[2], qrl[3]));
-                    st_chunk(sm + OFF_BD, c, j, make_uint4(kch[0], kch[1], kch[2], kch[3]));
-                    st_chunk(sm + OFF_BDLO, c, j, make_uint4(kcl[0], kcl[1], kcl[2], kcl[3]));
-                    st_chunk(sm + OFF_QG, c, j, make_uint4(gq[0], gq[1], gq[2], gq[3]));
-                    st_chunk(sm + OFF_KT, c, j, make_uint4(kt[0], kt[1], kt[2], kt[3]));
+                    const int chunk = 2 * rq + jj;
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        uint32_t krh[4], krl[4], qrh[4], qrl[4], kch[4], kcl[4], gq[4], kt[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            float vk[2], vq[2], vc[2];
+#pragma unroll
+                            for (int w = 0; w < 2; ++w) {
+                                const int w8 = 2 * e + w, rr = 8 * jj + w8, r = 16 * rq + rr;
+                                const bool act = (r >= lo && r < hi);
+                                const float kk = u ? hi_bf16(kp[w8]) : lo_bf16(kp[w8]);
+                                const float qq = u ? hi_bf16(qp[w8]) : lo_bf16(qp[w8]);
+                                const float gv = u ? Gq[rr].y : Gq[rr].x;
+                                const float x = basec[u] + gv - Rc[u];
+                                const float e1 = act ? ex2(x) : 0.f;
+                                const float e2 = act ? ex2(-x) : 0.f;
+                                vk[w] = kk * e1;
+                                vq[w] = qq * e1;
+                                vc[w] = kk * e2;
+                            }
+                            krh[e] = pack_bf16x2(vk[0], vk[1]);
+                            qrh[e] = pack_bf16x2(vq[0], vq[1]);
+                            kch[e] = pack_bf16x2(vc[0], vc[1]);
+                            krl[e] = pack_bf16x2(vk[0] - lo_bf16(krh[e]), vk[1] - hi_bf16(krh[e]));
+                            qrl[e] = pack_bf16x2(vq[0] - lo_bf16(qrh[e]), vq[1] - hi_bf16(qrh[e]));
+                            kcl[e] = pack_bf16x2(vc[0] - lo_bf16(kch[e]), vc[1] - hi_bf16(kch[e]));
+                            gq[e] = pack_f16x2(vq[0] * pRc[u], vq[1] * pRc[u]);
+                            kt[e] = pack_f16x2(vc[0] * pLc[u], vc[1] * pLc[u]);
+                        }
+                        const int c = 2 * cp + u;
+                        st_chunk(sm + OFF_AD, c, chunk, make_uint4(krh[0], krh[1], krh[2], krh[3]));
+                        st_chunk(sm + OFF_AD + 16384, c, chunk, make_uint4(qrh[0], qrh[1], qrh[2], qrh[3]));
+                        st_chunk(sm + OFF_ADLO, c, chunk, make_uint4(krl[0], krl[1], krl[2], krl[3]));
+                        st_chunk(sm + OFF_ADLO + 16384, c, chunk, make_uint4(qrl[0], qrl[1], qrl[2], qrl[3]));
+                        st_chunk(sm + OFF_BD, c, chunk, make_uint4(kch[0], kch[1], kch[2], kch[3]));
+                        st_chunk(sm + OFF_BDLO, c, chunk, make_uint4(kcl[0], kcl[1], kcl[2], kcl[3]));
+                        st_chunk(sm + OFF_QG, c, chunk, make_uint4(gq[0], gq[1], gq[2], gq[3]));
+                        st_chunk(sm + OFF_KT, c, chunk, make_uint4(kt[0], kt[1], kt[2], kt[3]));
+                    }
                 }
-                sGl[c] = exp2f(Glast);
-                sR[c] = pR;
-                if (c < kC) sBst[c] = (c >= lo && c < hi) ? sBin[c] : 0.f;
                 fence_proxy_async_smem();
-                named_bar_sync(1, 128);
-                if (ptid == 0) mbar_arrive(&X.bar[B_OPS]);
-                // Gram readout: rows 0..63 -> A (times beta, strictly lower),
-                // rows 64..127 -> P (lower including the diagonal).
-                if (!wg_wait(X, B_MMA_G, step, 1)) { alive = false; break; }
-                // The Gram has read the q/k/g staging area (lo parts): the next
-                // chunk may be loaded once the last pass is through.
-                if (ptid == 0 && p == npass - 1) mbar_arrive(&X.bar[B_QKG_EMPTY]);
+                group_sync();
+                if (ct == 0) mbar_arrive(&X.bar[B_OPS]);
+
+                // ---- while the Gram runs: the v tile to fp16 (first pass of a
+                // chunk) and the state decay with its fp16 copy.
+                const StepDesc d = X.desc[step & 1];
+                if (d.first_pass) {
+                    if (!group_wait(X, B_V_FULL, chunk_v)) { alive = false; break; }
+                    uint4* vt = reinterpret_cast<uint4*>(sm + OFF_V);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        uint4 x = vt[ct + 256 * u];
+                        x.x = bf16x2_to_f16x2(x.x);
+                        x.y = bf16x2_to_f16x2(x.y);
+                        x.z = bf16x2_to_f16x2(x.z);
+                        x.w = bf16x2_to_f16x2(x.w);
+                        vt[ct + 256 * u] = x;
+                    }
+                }
+                if (d.last_pass) ++chunk_v;
+                tc_fence_after();
+#pragma unroll
+                for (int jb = 0; jb < 2; ++jb) {
+                    const int c0 = 64 * half + 32 * jb;
+                    uint32_t r[32], b[16];
+                    tmem_ld32(tmem + lane_base + TM_S + c0, r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        b[i] = pack_f16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+                    tmem_st16(tmem + lane_base + TM_SB + (c0 >> 1), b);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        r[i] = __float_as_uint(__uint_as_float(r[i]) * sGl[c0 + i]);
+                    tmem_st32(tmem + lane_base + TM_S + c0, r);
+                }
+                tmem_st_wait();
+                fence_proxy_async_smem();                  // the converted v tile
+                tc_fence_before();
+
+                // ---- Gram readout: rows 0..63 -> A (times beta, strictly lower,
+                // fp32), rows 64..127 -> P (lower including the diagonal, fp16).
+                if (!group_wait(X, B_MMA_G, step)) { alive = false; break; }
                 tc_fence_after();
                 {
-                    uint32_t d0[32], d1[32];
-                    tmem_ld32(tmem + lane_base + TM_G, d0);
-                    tmem_ld32(tmem + lane_base + TM_G + 32, d1);
+                    uint32_t dg[32], dl[32];
+                    tmem_ld32(tmem + lane_base + TM_G + 32 * half, dg);
+                    tmem_ld32(tmem + lane_base + TM_G + 64 + 32 * half, dl);
                     tmem_ld_wait();
-                    if (c < kC) {
-                        const int r = c;
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        dg[i] = __float_as_uint(__uint_as_float(dg[i]) + __uint_as_float(dl[i]));
+                    if (L < kC) {
+                        const int r = L;
                         const bool act_r = (r >= lo && r < hi);
                         const float b = sBst[r];
 #pragma unroll
-                        for (int i = 0; i < kC; ++i) {
-                            const uint32_t raw = (i < 32) ? d0[i & 31] : d1[i & 31];
-                            const bool keep = act_r && i < r && i >= lo;
-                            sA[r * LDA + i] = keep ? b * __uint_as_float(raw) : 0.f;
+                        for (int i4 = 0; i4 < 8; ++i4) {
+                            float v4[4];
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) {
+                                const int i = 32 * half + 4 * i4 + u;
+                                const bool keep = act_r && i < r && i >= lo;
+                                v4[u] = keep ? b * __uint_as_float(dg[4 * i4 + u]) : 0.f;
+                            }
+                            *reinterpret_cast<float4*>(sA + r * LDA + 32 * half + 4 * i4) =
+                                make_float4(v4[0], v4[1], v4[2], v4[3]);
                         }
                     } else {
-                        const int r = c - kC;
+                        const int r = L - kC;
                         const bool act_r = (r >= lo && r < hi);
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) {
+                        for (int j = 0; j < 4; ++j) {
                             uint32_t pk[4];
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
                                 float pv[2];
 #pragma unroll
                                 for (int u = 0; u < 2; ++u) {
-                                    const int i = j * 8 + e * 2 + u;
-                                    const uint32_t raw = (i < 32) ? d0[i & 31] : d1[i & 31];
+                                    const int i = 32 * half + 8 * j + 2 * e + u;
                                     const bool keep = act_r && i <= r && i >= lo;
-                                    pv[u] = keep ? __uint_as_float(raw) : 0.f;
+                                    pv[u] = keep ? __uint_as_float(dg[8 * j + 2 * e + u]) : 0.f;
                                 }
                                 pk[e] = pack_f16x2(pv[0], pv[1]);
                             }
-                            st_chunk(sm + OFF_P, r, j, make_uint4(pk[0], pk[1], pk[2], pk[3]));
+                            st_chunk(sm + OFF_P, r, 4 * half + j, make_uint4(pk[0], pk[1], pk[2], pk[3]));
                         }
                     }
                 }
                 tc_fence_before();
-                named_bar_sync(1, 128);
-                ut_solve(sA, sY, ptid, 1);
-                {   // T = X Diag(beta) -> bf16 (W product) and fp16 (V product) rows
-                    const int r = ptid >> 1, half = ptid & 1;
+                group_sync();
+                // ---- UT solve, S1: diagonal-block inverses D (warps of ct < 128),
+                // A_off as fp16 and identity rows in TMEM (the other warps).
+                if (ct < 128) {
+                    const int b = ct >> 5, j = ct & 31;
+                    float x[16];
+                    diag_block_column(sA, b, j, x);
+                    if (j < 16) {
+                        const int k = 16 * b + j;        // column k of D = row k of the tiles
+                        const float bk = sBst[k];
+#pragma unroll
+                        for (int c8 = 0; c8 < 8; ++c8) {
+                            uint32_t pd[4], pp[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                float dv[2];
+#pragma unroll
+                                for (int u = 0; u < 2; ++u) {
+                                    const int r = 8 * c8 + 2 * e + u;
+                                    dv[u] = ((r >> 4) == b) ? x[r & 15] : 0.f;
+                                }
+                                pd[e] = pack_f16x2(dv[0], dv[1]);
+                                pp[e] = pack_f16x2(dv[0] * bk, dv[1] * bk);
+                            }
+                            st_chunk(sm + OFF_DM, k, c8, make_uint4(pd[0], pd[1], pd[2], pd[3]));
+                            st_chunk(sm + OFF_DPK, k, c8, make_uint4(pp[0], pp[1], pp[2], pp[3]));
+                        }
+                    }
+                } else {
+                    const int k = (ct - 128) >> 1, hh = ct & 1;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        uint32_t pk[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int c0 = 32 * hh + 8 * j + 2 * e;
+                            const float a0 = ((c0 >> 4) < (k >> 4)) ? sA[k * LDA + c0] : 0.f;
+                            const float a1 = (((c0 + 1) >> 4) < (k >> 4)) ? sA[k * LDA + c0 + 1] : 0.f;
+                            pk[e] = pack_f16x2(a0, a1);
+                        }
+                        st_chunk(sm + OFF_AO, k, 4 * hh + j, make_uint4(pk[0], pk[1], pk[2], pk[3]));
+                    }
+                    if ((warp & 3) < 2) {                // lanes 0..63: identity rows
+                        uint32_t id[32];
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            id[i] = ((2 * i == L) ? 0x3C00u : 0u) | ((2 * i + 1 == L) ? 0x3C000000u : 0u);
+                        tmem_st32(tmem + lane_base + TM_IA, id);
+                        tmem_st_wait();
+                    }
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                group_sync();
+                if (ct == 0) mbar_arrive(&X.bar[B_S1]);
+                const bool top = (warp & 3) < 2;         // this warp holds rows 0..63
+                // S2: N -> fp16 A operand (TMEM) and MN-major B tile
+                if (!group_wait(X, B_R1, step)) { alive = false; break; }
+                tc_fence_after();
+                if (top) {
+                    uint32_t nb[16];
+                    tmem_row_f16(tmem + lane_base + TM_N + 32 * half, nb);
+                    tmem_st16(tmem + lane_base + TM_NA + 16 * half, nb);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        st_chunk(sm + OFF_NB, L, 4 * half + j,
+                                 make_uint4(nb[4 * j], nb[4 * j + 1], nb[4 * j + 2], nb[4 * j + 3]));
+                    tmem_st_wait();
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                group_sync();
+                if (ct == 0) mbar_arrive(&X.bar[B_S2]);
+                // S3: N^2 -> fp16 A operand
+                if (!group_wait(X, B_R2, step)) { alive = false; break; }
+                tc_fence_after();
+                if (top) {
+                    uint32_t nb[16];
+                    tmem_row_f16(tmem + lane_base + TM_N2 + 32 * half, nb);
+                    tmem_st16(tmem + lane_base + TM_N2A + 16 * half, nb);
+                    tmem_st_wait();
+                }
+                tc_fence_before();
+                group_sync();
+                if (ct == 0) mbar_arrive(&X.bar[B_S3]);
+                // S4: Y -> fp16 MN-major B tile (Y stays in TMEM as the accumulator)
+                if (!group_wait(X, B_R3, step)) { alive = false; break; }
+                // The g tile's space is no longer read: the next chunk may load.
+                if (ct == 0 && d.last_pass) mbar_arrive(&X.bar[B_QKG_EMPTY]);
+                tc_fence_after();
+                if (top) {
+                    uint32_t yb[16];
+                    tmem_row_f16(tmem + lane_base + TM_N2 + 32 * half, yb);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        st_chunk(sm + OFF_YB, L, 4 * half + j,
+                                 make_uint4(yb[4 * j], yb[4 * j + 1], yb[4 * j + 2], yb[4 * j + 3]));
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                group_sync();
+                if (ct == 0) mbar_arrive(&X.bar[B_S4]);
+                // S5: T -> bf16 (W product) and fp16 (V product) rows
+                if (!group_wait(X, B_R4, step)) { alive = false; break; }
+                tc_fence_after();
+                if (top) {
+                    uint32_t d[32];
+                    tmem_ld32(tmem + lane_base + TM_N2 + 32 * half, d);
+                    tmem_ld_wait();
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         uint32_t pb[4], ph[4];
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            const int i0 = half * 32 + j * 8 + e * 2;
-                            const float t0v = x_at(sA, r, i0) * sBst[i0];
-                            const float t1v = x_at(sA, r, i0 + 1) * sBst[i0 + 1];
+                            const float t0v = __uint_as_float(d[8 * j + 2 * e]);
+                            const float t1v = __uint_as_float(d[8 * j + 2 * e + 1]);
                             pb[e] = pack_bf16x2(t0v, t1v);
                             ph[e] = pack_f16x2(t0v, t1v);
                         }
-                        st_chunk(sm + OFF_T, r, half * 4 + j, make_uint4(pb[0], pb[1], pb[2], pb[3]));
-                        st_chunk(sm + OFF_T16, r, half * 4 + j, make_uint4(ph[0], ph[1], ph[2], ph[3]));
+                        st_chunk(sm + OFF_T, L, 4 * half + j, make_uint4(pb[0], pb[1], pb[2], pb[3]));
+                        st_chunk(sm + OFF_T16, L, 4 * half + j, make_uint4(ph[0], ph[1], ph[2], ph[3]));
                     }
                 }
                 fence_proxy_async_smem();
-                named_bar_sync(1, 128);
-                if (ptid == 0) mbar_arrive(&X.bar[B_T]);
-                // W readout: -W^T row c = -2^R_c x (Kr^T T^T) row c, as fp16
-                if (!wg_wait(X, B_MMA_W, step, 1)) { alive = false; break; }
+                tc_fence_before();
+                group_sync();
+                if (ct == 0) mbar_arrive(&X.bar[B_T]);
+
+                // ---- W readout: -W^T row c = -2^R_c x (Kr^T T^T) row c, fp16
+                if (!group_wait(X, B_MMA_W, step)) { alive = false; break; }
                 tc_fence_after();
                 {
-                    uint32_t d0[32], d1[32];
-                    tmem_ld32(tmem + lane_base + TM_W, d0);
-                    tmem_ld32(tmem + lane_base + TM_W + 32, d1);
+                    uint32_t dw[32];
+                    tmem_ld32(tmem + lane_base + TM_W + 32 * half, dw);
                     tmem_ld_wait();
-                    const float sc = -pR;
+                    const float sc = -sR[L];
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
+                    for (int j = 0; j < 4; ++j) {
                         uint32_t pk[4];
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int i = j * 8 + e * 2;
-                            const uint32_t r0 = (i < 32) ? d0[i & 31] : d1[i & 31];
-                            const uint32_t r1 = (i + 1 < 32) ? d0[(i + 1) & 31] : d1[(i + 1) & 31];
-                            pk[e] = pack_f16x2(sc * __uint_as_float(r0), sc * __uint_as_float(r1));
-                        }
-                        st_chunk(sm + OFF_WT, c, j, make_uint4(pk[0], pk[1], pk[2], pk[3]));
+                        for (int e = 0; e < 4; ++e)
+                            pk[e] = pack_f16x2(sc * __uint_as_float(dw[8 * j + 2 * e]),
+                                               sc * __uint_as_float(dw[8 * j + 2 * e + 1]));
+                        st_chunk(sm + OFF_WT, L, 4 * half + j, make_uint4(pk[0], pk[1], pk[2], pk[3]));
                     }
                 }
                 tc_fence_before();
                 fence_proxy_async_smem();
-                named_bar_sync(1, 128);
-                if (ptid == 0) mbar_arrive(&X.bar[B_W]);
+                group_sync();
+                if (ct == 0) mbar_arrive(&X.bar[B_CV]);
+
+                // ---- U^T -> fp16 A operand
+                if (!group_wait(X, B_MMA_C, step)) { alive = false; break; }
+                tc_fence_after();
+                {
+                    uint32_t du[32], b[16];
+                    tmem_ld32(tmem + lane_base + TM_C + 32 * half, du);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        b[i] = pack_f16x2(__uint_as_float(du[2 * i]), __uint_as_float(du[2 * i + 1]));
+                    tmem_st16(tmem + lane_base + TM_UB + 16 * half, b);
+                    tmem_st_wait();
+                }
+                tc_fence_before();
+                group_sync();
+                if (ct == 0) mbar_arrive(&X.bar[B_U]);
+
+                // ---- O^T readout.  A full single-pass chunk with bf16 output is
+                // staged in shared memory (the A/X region, idle until the next
+                // chunk's Gram operands) and written by one TMA tensor store; other
+                // chunks (a ragged tail, the two passes of a wide chunk, fp32
+                // output) are stored by the threads.
+                if (!group_wait(X, B_MMA_OS, step)) { alive = false; break; }
+                tc_fence_after();
+                {
+                    uint32_t dd[32];
+                    tmem_ld32(tmem + lane_base + TM_O + 32 * half, dd);
+                    tmem_ld_wait();
+                    const bool tma_out = (sizeof(TO) == 2) && d.lo == 0 && d.hi == kC;
+                    if (tma_out) {
+                        uint8_t* stg = sm + OFF_OST;
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            const int r = 32 * half + i;
+                            *reinterpret_cast<__nv_bfloat16*>(stg + r * 256 + 2 * L) =
+                                __float2bfloat16_rn(__uint_as_float(dd[i]));
+                        }
+                        fence_proxy_async_smem();
+                        tc_fence_before();
+                        group_sync();
+                        if (ct == 0) {
+                            tma_store_2d(&tm_o, h * kD, d.t0, stg);
+                            bulk_commit_group();
+                        }
+                    } else {
+                        TO* op = o + ((long long)d.t0 * H + h) * kD + L;
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            const int r = 32 * half + i;
+                            if (r >= d.lo && r < d.hi)
+                                out_store(op + (long long)r * H * kD, __uint_as_float(dd[i]));
+                        }
+                        tc_fence_before();
+                    }
+                }
                 ++step;
             }
         }
-    } else {
-        // ------------------------------------------------------- consumer
-        const int v = ((warp & 3) << 5) | lane;           // value column == TMEM lane
-        const int ctid = tid - 192;                       // 0..127 within the group
-        const uint32_t lane_base = (uint32_t)((warp & 3) << 5) << 16;
-        const float* sGl = reinterpret_cast<const float*>(sm + OFF_GL);
-        // S^T <- S0^T (row v of S^T is column v of S0)
-#pragma unroll
-        for (int jb = 0; jb < 4; ++jb) {
-            uint32_t r[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-                r[i] = __float_as_uint(S0 ? S0[sbase + (long long)(jb * 32 + i) * kD + v] : 0.f);
-            tmem_st32(tmem + lane_base + TM_S + jb * 32, r);
-        }
-        tmem_st_wait();
-        int chunk_v = 0;
-        for (int step = 0; nch > 0; ++step) {
-            if (!wg_wait(X, B_OPS, step, 2)) break;
-            const StepDesc d = X.desc[step & 1];
-            if (d.first_pass) {
-                // The chunk's v tile: bf16 -> fp16 in place (same element layout).
-                if (!wg_wait(X, B_V_FULL, chunk_v, 2)) break;
-                uint4* vt = reinterpret_cast<uint4*>(sm + OFF_V);
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    uint4 x = vt[ctid + 128 * u];
-                    x.x = bf16x2_to_f16x2(x.x);
-                    x.y = bf16x2_to_f16x2(x.y);
-                    x.z = bf16x2_to_f16x2(x.z);
-                    x.w = bf16x2_to_f16x2(x.w);
-                    vt[ctid + 128 * u] = x;
-                }
-                fence_proxy_async_smem();
-            }
-            if (d.last_pass) ++chunk_v;
-            tc_fence_after();
-            // decay pass: fp16 copy of S^T for this step's products, then
-            // S^T <- S^T Diag(e^{G_last}).
-#pragma unroll
-            for (int jb = 0; jb < 4; ++jb) {
-                uint32_t r[32], b[16];
-                tmem_ld32(tmem + lane_base + TM_S + jb * 32, r);
-                tmem_ld_wait();
-#pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    b[i] = pack_f16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
-                tmem_st16(tmem + lane_base + TM_SB + jb * 16, b);
-#pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    r[i] = __float_as_uint(__uint_as_float(r[i]) * sGl[jb * 32 + i]);
-                tmem_st32(tmem + lane_base + TM_S + jb * 32, r);
-            }
-            tmem_st_wait();
-            tc_fence_before();
-            named_bar_sync(2, 128);
-            if (ctid == 0) mbar_arrive(&X.bar[B_S]);
-            // U^T -> fp16 A operand
-            if (!wg_wait(X, B_MMA_C, step, 2)) break;
-            tc_fence_after();
-            {
-                uint32_t d0[32], d1[32], b[32];
-                tmem_ld32(tmem + lane_base + TM_C, d0);
-                tmem_ld32(tmem + lane_base + TM_C + 32, d1);
-                tmem_ld_wait();
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    b[i] = pack_f16x2(__uint_as_float(d0[2 * i]), __uint_as_float(d0[2 * i + 1]));
-                    b[16 + i] = pack_f16x2(__uint_as_float(d1[2 * i]), __uint_as_float(d1[2 * i + 1]));
-                }
-                tmem_st32(tmem + lane_base + TM_UB, b);
-                tmem_st_wait();
-            }
-            tc_fence_before();
-            named_bar_sync(2, 128);
-            if (ctid == 0) mbar_arrive(&X.bar[B_U]);
-            // O^T readout
-            if (!wg_wait(X, B_MMA_OS, step, 2)) break;
-            tc_fence_after();
-            {
-                uint32_t d0[32], d1[32];
-                tmem_ld32(tmem + lane_base + TM_O, d0);
-                tmem_ld32(tmem + lane_base + TM_O + 32, d1);
-                tmem_ld_wait();
-                TO* op = o + ((long long)d.t0 * H + h) * kD + v;
-#pragma unroll
-                for (int r = 0; r < kC; ++r) {
-                    if (r >= d.lo && r < d.hi)
-                        out_store(op + (long long)r * H * kD,
-                                  __uint_as_float(r < 32 ? d0[r & 31] : d1[r & 31]));
-                }
-            }
-            tc_fence_before();
-            named_bar_sync(2, 128);
-            if (ctid == 0) mbar_arrive(&X.bar[B_O_FREE]);
-            if (d.last_step) break;
-        }
+        if (ct == 0) bulk_wait_group0();                   // the last O store has landed
         if (S_final && !*reinterpret_cast<volatile int32_t*>(&X.misc->abort)) {
             tc_fence_after();
 #pragma unroll
-            for (int jb = 0; jb < 4; ++jb) {
+            for (int jb = 0; jb < 2; ++jb) {
                 uint32_t r[32];
-                tmem_ld32(tmem + lane_base + TM_S + jb * 32, r);
+                tmem_ld32(tmem + lane_base + TM_S + 64 * half + 32 * jb, r);
                 tmem_ld_wait();
 #pragma unroll
                 for (int i = 0; i < 32; ++i)
-                    S_final[sbase + (long long)(jb * 32 + i) * kD + v] = __uint_as_float(r[i]);
+                    S_final[sbase + (long long)(64 * half + 32 * jb + i) * kD + L] = __uint_as_float(r[i]);
             }
         }
     }
@@ -759,8 +986,13 @@ cudaError_t launch_typed(const void* q, const void* k, const void* v, const floa
                          int64_t T, int32_t H, void* o, float* S_final, int32_t* ws,
                          cudaStream_t stream)
 {
-    CUtensorMap mq, mk, mg, mv;
+    CUtensorMap mq, mk, mg, mv, mo;
+    // The output map is used for bf16 output only (fp32 output is stored by
+    // the threads); for fp32 a copy of the q map fills the slot.
+    const bool bf16_out = sizeof(TO) == 2;
     if (!make_map(&mq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, T, kD, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        (bf16_out && !make_map(&mo, o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, T, kD,
+                               CU_TENSOR_MAP_SWIZZLE_NONE)) ||
         !make_map(&mk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, T, kD, CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !make_map(&mg, g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, H, T, kD, CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !make_map(&mv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, T, 64, CU_TENSOR_MAP_SWIZZLE_128B))
@@ -780,7 +1012,8 @@ cudaError_t launch_typed(const void* q, const void* k, const void* v, const floa
     }
     const long long blocks = (long long)N * H;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    kern<<<(unsigned)blocks, kThreads, kSmemBytes, stream>>>(mq, mk, mg, mv, beta, S0, cu, ws,
+    if (!bf16_out) mo = mq;
+    kern<<<(unsigned)blocks, kThreads, kSmemBytes, stream>>>(mq, mk, mg, mv, mo, beta, S0, cu, ws,
                                                             (long long)T, H,
                                                             static_cast<TO*>(o), S_final);
     const cudaError_t e = cudaGetLastError();
