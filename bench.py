@@ -277,9 +277,10 @@ def run_reference(args):
 # --------------------------------------------------------------------------
 # the CUDA path
 # --------------------------------------------------------------------------
-PREFILL_SOURCES = ["gated_delta_rule_05_gb300/csrc/kda_prefill_simt.cu",
+PREFILL_SOURCES = ["gated_delta_rule_05_gb300/csrc/kda_prefill_tc.cu",
+                   "gated_delta_rule_05_gb300/csrc/kda_sm100.cuh",
                    "gated_delta_rule_05_gb300/csrc/kda_internal.cuh"]
-PREFILL_KERNEL = "prefill_simt_kernel"
+PREFILL_KERNEL = "prefill_tc_kernel"
 DECODE_SOURCES = ["gated_delta_rule_05_gb300/csrc/kda_decode.cu",
                   "gated_delta_rule_05_gb300/csrc/kda_internal.cuh"]
 DECODE_KERNEL = "decode_kernel"
@@ -303,9 +304,40 @@ def run_kda(args):
     peaks = load_peaks()
     stream = torch.cuda.current_stream(dev)
 
-    # ---------------- prefill ----------------
+    line = {}
+    smi_id = gpu_id_for_smi(torch, local)
+    if args.only in ("all", "prefill"):
+        line.update(bench_prefill(args, kda, torch, synth, peaks, stream, dev, rank, world, smi_id))
+    if args.only in ("all", "decode"):
+        line["decode"] = bench_decode(args, kda, torch, synth, peaks, stream, dev, rank, world, smi_id)
+    if rank == 0:
+        if "value" not in line:        # decode only: its metric leads the line
+            d = line["decode"]
+            line.update({"metric": METRIC, "value": d["value"], "unit": "GB/s", "n_gpus": world,
+                         "steps": args.steps, "warmup": args.warmup,
+                         "ms_per_step": d["ms_per_step"], "higher_is_better": True,
+                         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+                         "data": "synthetic", "config": {"workload": "decode_1024x32"},
+                         "roofline": d["roofline"], "clocks": d["clocks"],
+                         "gpu_launches": d["gpu_launches"], "cpu_baseline": None,
+                         "e2e": None})
+        else:
+            line["gpu_launches"] = line.get("gpu_launches", 0) + \
+                line.get("decode", {}).get("gpu_launches", 0)
+        if args.only == "all" and world == 1 and not args.no_cpu:
+            line["cpu_baseline"] = cpu_baseline()   # rank 0 at N=1 only
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def bench_prefill(args, kda, torch, synth, peaks, stream, dev, rank, world, smi_id):
     wp = synth.WORKLOADS[PREFILL_WORKLOAD]
-    inp = synth.generate(synth.draw_lengths(wp), wp.H, wp.d, wp.d, dtype=wp.dtype,
+    lengths = [args.tokens] if args.tokens else synth.draw_lengths(wp)
+    workload = wp.name if not args.tokens else "prefill_h32_t%d" % args.tokens
+    inp = synth.generate(lengths, wp.H, wp.d, wp.d, dtype=wp.dtype,
                          gate=wp.gate, q_scale=wp.q_scale, s0_std=wp.s0_std,
                          seed=rank_seed(wp.seed, rank), device=dev)
     T, H, d = inp.q.shape
@@ -322,7 +354,6 @@ def run_kda(args):
     torch.cuda.synchronize(dev)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
-    smi_id = gpu_id_for_smi(torch, local)
     barrier(world)
     torch.cuda.synchronize(dev)
     with ClockSampler(smi_id) as clk:
@@ -343,21 +374,34 @@ def run_kda(args):
     alg_bytes = T * H * BYTES_PER_TOKEN_HEAD
     alg_flops = T * H * FLOPS_PER_TOKEN_HEAD
     achieved = alg_bytes / (launch_ms / 1e3) / 1e9
-    traffic = committed_traffic("prefill_h32_t1m/" + PREFILL_KERNEL, PREFILL_SOURCES)
+    traffic = committed_traffic(workload + "/" + PREFILL_KERNEL, PREFILL_SOURCES)
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
                 "peak_source": peaks["source"], "kernel": PREFILL_KERNEL,
                 "algorithmic_bytes_per_launch": alg_bytes,
                 "tensor_tflops_achieved": alg_flops / (launch_ms / 1e3) / 1e12,
                 "tensor_frac": (alg_flops / (launch_ms / 1e3) / 1e12) / peaks["bf16_tflops"]}
-    clocks = clk.summary()
+    out = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": workload, "num_seqs": 1, "seq_len": T, "H": H,
+                   "d_k": d, "d_v": d, "io_dtype": "bf16", "state_dtype": "fp32",
+                   "tokens_per_step_per_gpu": T, "parallelism": "dp%d" % world,
+                   "l2": "inputs larger than L2 (%.1f GB per step)" % (alg_bytes / 1e9)},
+        "roofline": roofline,
+        # per prefill call: the varlen work-list kernel + the tensor-core kernel
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk.summary(),
+        "wall_s_timed_prefill": t_wall,
+    }
+    if not args.no_e2e:
+        out["e2e"] = run_e2e(kda, torch, inp, dev, stream, args, world)
+    return out
 
-    # ---------------- e2e: host buffers through the public API ----------------
-    e2e = run_e2e(kda, torch, inp, dev, stream, args, world)
-    del inp, o
-    torch.cuda.empty_cache()
 
-    # ---------------- decode ----------------
+def bench_decode(args, kda, torch, synth, peaks, stream, dev, rank, world, smi_id):
     wd = synth.WORKLOADS[DECODE_WORKLOAD]
     dinp = synth.generate(synth.draw_lengths(wd), wd.H, wd.d, wd.d, dtype=wd.dtype,
                           gate=wd.gate, q_scale=wd.q_scale, s0_std=wd.s0_std,
@@ -390,7 +434,7 @@ def run_kda(args):
     dec_bytes = units * decode_bytes_per_unit(wd.d)
     dec_gbs_all = dec_bytes * world * args.steps / (dec_ms_max / 1e3) / 1e9
     dec_achieved = dec_bytes / (dec_ms / args.steps / 1e3) / 1e9
-    decode_obj = {
+    return {
         "value": dec_gbs_all, "unit": "GB/s", "ms_per_step": dec_ms_max / args.steps,
         "workload": "decode_1024x32", "tokens_per_step": Nd * world,
         "roofline": {"bound": "hbm", "achieved": dec_achieved, "peak": peaks["hbm_gbs"],
@@ -399,34 +443,9 @@ def run_kda(args):
                                                   DECODE_SOURCES),
                      "peak_source": peaks["source"], "kernel": DECODE_KERNEL,
                      "algorithmic_bytes_per_launch": dec_bytes},
+        "gpu_launches": args.steps,
         "clocks": dclk.summary(),
     }
-
-    if rank != 0:
-        return 0
-    cpu = cpu_baseline() if world == 1 else None   # rank 0 at N=1 only
-    line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": "prefill_h32_t1m", "num_seqs": 1, "seq_len": T, "H": H,
-                   "d_k": d, "d_v": d, "io_dtype": "bf16", "state_dtype": "fp32",
-                   "tokens_per_step_per_gpu": T, "parallelism": "dp%d" % world,
-                   "l2": "inputs larger than L2 (%.1f GB per step)" % (alg_bytes / 1e9)},
-        "roofline": roofline,
-        "cpu_baseline": cpu,
-        "e2e": e2e,
-        "gpu_launches": 2 * args.steps,   # per prefill: the varlen work-list kernel + the prefill kernel
-        "clocks": clocks,
-        "decode": decode_obj,
-        "wall_s_timed_prefill": t_wall,
-    }
-    print(json.dumps(line), flush=True)
-    if world > 1:
-        import torch.distributed as dist
-        dist.destroy_process_group()
-    return 0
 
 
 def host_memory_available():
@@ -526,6 +545,12 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["kda", "reference"], default="kda")
+    ap.add_argument("--only", choices=["all", "prefill", "decode"], default="all",
+                    help="time only one part (profiling runs)")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="prefill length override (profiling runs on a smaller case)")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU baseline")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "kda":
         print("bench.py: note: fewer than 3 warm-up steps", file=sys.stderr)
