@@ -2,7 +2,29 @@
 // dispatch to the kernels, status mapping.  No allocation, no host sync.
 #include <stdint.h>
 
+#include <mutex>
+
 #include "kda_internal.cuh"
+
+namespace kda {
+
+int device_sm_count()
+{
+    constexpr int kMaxDevices = 64;
+    static std::mutex mu;
+    static int cached[kMaxDevices] = {};
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cached[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        cached[dev] = n;
+    }
+    return cached[dev];
+}
+
+}  // namespace kda
 
 namespace {
 
@@ -29,9 +51,9 @@ extern "C" {
 size_t kda_prefill_workspace_bytes(int32_t num_seqs, int32_t H, int32_t d_k,
                                    int32_t d_v)
 {
-    (void)H;
-    (void)d_k;
-    (void)d_v;
+    kda::SplitPlan plan;
+    if (d_k == 128 && d_v == 128 && kda::split_plan(num_seqs, H, kda::device_sm_count(), &plan))
+        return plan.bytes;
     return kda::workspace_bytes(num_seqs);
 }
 
@@ -68,11 +90,29 @@ kda_status_t kda_prefill(const void* q, const void* k, const void* v,
 
     int32_t* ws = static_cast<int32_t*>(workspace);
     cudaError_t err = cudaSuccess;
-    if (cu_seqlens) {
-        err = kda::launch_worklist(cu_seqlens, num_seqs, total_tokens, ws, stream);
+    const bool tc = kda::prefill_tc_supported(dtype, d_k, total_tokens);
+    // Few (sequence, head) units and a workspace with room for the ring: the
+    // producer / consumer kernel.
+    kda::SplitPlan plan;
+    const bool split = tc && kda::split_plan(num_seqs, H, kda::device_sm_count(), &plan) &&
+                       workspace_bytes >= plan.bytes;
+    if (cu_seqlens || split) {
+        int32_t* flags =
+            split ? reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + plan.flags_off)
+                  : nullptr;
+        const int32_t nflags = split ? plan.units * (plan.ring + 1) : 0;
+        err = kda::launch_worklist(cu_seqlens, num_seqs, total_tokens, ws, flags, nflags, stream);
         if (err != cudaSuccess) return KDA_ERR_CUDA;
     }
-    if (kda::prefill_tc_supported(dtype, d_k, total_tokens))
+    if (split) {
+        err = kda::launch_prefill_split(q, k, v, log_alpha, beta, S0, cu_seqlens, num_seqs,
+                                        total_tokens, H, dtype, o, S_final, ws, plan, stream);
+        if (err == cudaSuccess) return KDA_OK;
+        // The launch was refused (a configuration error, nothing ran): the
+        // single-CTA kernel computes the same result.
+        (void)cudaGetLastError();
+    }
+    if (tc)
         err = kda::launch_prefill_tc(q, k, v, log_alpha, beta, S0, cu_seqlens, num_seqs,
                                      total_tokens, H, dtype, o, S_final, ws, stream);
     else

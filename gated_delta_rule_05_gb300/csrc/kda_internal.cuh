@@ -15,11 +15,21 @@ namespace kda {
 //   byte 0   : int32 work counter (persistent kernels take items from it)
 //   byte 4   : int32 error word (nonzero => cu_seqlens violated its contract)
 //   byte 8   : int32 timeout word (bit 1 set => a device-side wait gave up)
+//   byte 12  : int32 longest sequence length (written by the work-list kernel)
+//   byte 16  : int64 job counter of the split kernel's producers
+//   byte 24  : int32 abort word of the split kernel (nonzero => a CTA gave up
+//              and the others stop); cleared by the work-list kernel
 //   byte 256 : int32 order[N], sequence indices, longest first
+// and, when the split kernel is used (split_plan below), after order[]:
+//   flags    : int32 full[U][R], int32 consumed[U]   (U = N H units, R = ring depth)
+//   ring     : [U][R][2 steps][kSplitStepBytes] chunk operands, 1024-aligned
 constexpr size_t kWsHeaderBytes = 256;
 constexpr int kWsCounterWord = 0;
 constexpr int kWsErrorWord = 1;
 constexpr int kWsTimeoutWord = 2;
+constexpr int kWsMaxLenWord = 3;
+constexpr int kWsJobWord = 4;          // 64-bit, words 4 and 5
+constexpr int kWsAbortWord = 6;
 // Sequences are ordered longest-first when N <= this; above it the order is
 // the input order (the rank sort is O(N^2) on one CTA).
 constexpr int kMaxSortedSeqs = 2048;
@@ -29,6 +39,42 @@ inline size_t workspace_bytes(int32_t num_seqs) {
     size_t order = ((size_t)num_seqs * sizeof(int32_t) + 255) / 256 * 256;
     return kWsHeaderBytes + order;
 }
+
+// The split (producer / consumer) tensor-core prefill: one consumer CTA per
+// (sequence, head) unit and `producers` CTAs on the other SMs, handing chunk
+// operands over through a ring of `ring` chunk slots per unit in the
+// workspace.  Used when the units fill at most half of the SMs.
+constexpr size_t kSplitStepBytes = 66560;       // one step's operand block (65 KB)
+constexpr int kSplitMaxRing = 32;
+
+struct SplitPlan {
+    int32_t units, producers, ring;
+    size_t flags_off, ring_off, bytes;
+};
+
+inline bool split_plan(int32_t num_seqs, int32_t H, int sms, SplitPlan* plan) {
+    if (num_seqs < 1 || H < 1 || sms < 3) return false;
+    const long long units = (long long)num_seqs * H;
+    if (units > sms / 2) return false;
+    SplitPlan p;
+    p.units = (int32_t)units;
+    p.producers = sms - p.units;
+    // Producers claim chunks in chunk-major order, so about producers / units
+    // chunks of each unit are in flight; the ring holds twice that.
+    const int ahead = (p.producers + p.units - 1) / p.units;
+    p.ring = 2 * ahead + 2;
+    if (p.ring < 4) p.ring = 4;
+    if (p.ring > kSplitMaxRing) p.ring = kSplitMaxRing;
+    p.flags_off = workspace_bytes(num_seqs);
+    const size_t nflags = (size_t)p.units * (p.ring + 1);
+    p.ring_off = (p.flags_off + nflags * sizeof(int32_t) + 1023) / 1024 * 1024;
+    p.bytes = p.ring_off + (size_t)p.units * p.ring * 2 * kSplitStepBytes;
+    *plan = p;
+    return true;
+}
+
+// Number of SMs of the current device (cached per device; 0 on failure).
+int device_sm_count();
 
 // KDA_DEBUG set in the environment: failing host-side steps are reported on
 // stderr (the status codes stay the same).
@@ -41,8 +87,11 @@ __device__ __forceinline__ void st_f(float* p, float x) { *p = x; }
 __device__ __forceinline__ void st_f(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
 
 // Launchers (return cudaGetLastError() after enqueueing).
+// Validates cu_seqlens (when given), writes order[], the error word and the
+// longest length, resets the counters and zeroes `nflags` words at `flags`.
 cudaError_t launch_worklist(const int32_t* cu_seqlens, int32_t num_seqs,
-                            int64_t total_tokens, int32_t* ws, cudaStream_t stream);
+                            int64_t total_tokens, int32_t* ws, int32_t* flags,
+                            int32_t nflags, cudaStream_t stream);
 
 cudaError_t launch_decode(const void* q, const void* k, const void* v,
                           const float* log_alpha, const float* beta, float* S,
@@ -67,5 +116,12 @@ cudaError_t launch_prefill_tc(const void* q, const void* k, const void* v,
                               const int32_t* cu_seqlens, int32_t num_seqs, int64_t total_tokens,
                               int32_t H, kda_dtype_t dtype, void* o, float* S_final,
                               int32_t* ws, cudaStream_t stream);
+
+cudaError_t launch_prefill_split(const void* q, const void* k, const void* v,
+                                 const float* log_alpha, const float* beta, const float* S0,
+                                 const int32_t* cu_seqlens, int32_t num_seqs,
+                                 int64_t total_tokens, int32_t H, kda_dtype_t dtype, void* o,
+                                 float* S_final, int32_t* ws, const SplitPlan& plan,
+                                 cudaStream_t stream);
 
 }  // namespace kda

@@ -1,0 +1,566 @@
+// kda_prefill_split.cu -- the producer / consumer tensor-core prefill for
+// batches with few (sequence, head) units (bf16 q/k/v, d_k = d_v = 128).
+//
+// Why.  A chunk step of the chunkwise form ("Kimi 모델 분석", rlaope.github.io,
+// section "순환을 GPU에 올리기") is a chain of dependent phases, and only the
+// state carries from one chunk to the next.  Most of the chain (gate prep, the
+// Gram products, the UT solve, W: the front phases of kda_tc_chunk.cuh) does
+// not involve the state at all, so with one CTA per unit a batch of a few long
+// sequences keeps only a few SMs busy, each waiting on its own chain.  Here the
+// front phases of every chunk run on producer CTAs spread over the rest of the
+// GPU, and the CTA that owns a unit's state (its consumer) runs only the back
+// phases: state decay, U, O and the state update, about a fifth of the chain.
+//
+// Grid: one cooperative launch of exactly one CTA per SM (every CTA resident,
+// so CTAs may wait on one another).  CTA b < U is the consumer of unit b (the
+// b-th (sequence, head) pair, sequences longest first); the others are
+// producers.  All CTAs have the same 320 threads: warp 0 moves data, warp 1
+// issues the tensor-core products, warps 2..9 are the compute group.
+//
+// Hand-over.  Producers claim jobs (chunk c of unit u) from a 64-bit counter
+// in chunk-major order (job j = c U + u) and write the chunk's back-phase
+// operands (-W^T, (e^G Q)^T, P, Ktil^T, T as fp16 tiles in the 128-byte
+// swizzled layout of the MMA descriptors, and e^{G_last}) straight from
+// registers into slot c mod R of the unit's ring in the workspace; a chunk
+// whose decay span needs two passes fills two step blocks.  The producer's
+// data-movement warp then publishes the slot: fence, then a release store of
+// full[u][slot] = 2 (c + 1) + (passes - 1).  The consumer's loader polls that
+// word with acquire loads, copies each step block into one of two shared-
+// memory stages with one bulk copy, and the consumer records consumed[u] = c + 1
+// once the copy has landed.  A producer writes a slot only when consumed[u]
+// shows that the chunk R places earlier has left it.
+//
+// Progress.  Jobs are claimed in order and every job depends only on jobs of
+// earlier chunks, and a producer publishes a job before it waits for the slot
+// of its next one; the earliest unfinished job therefore always runs, so the
+// launch cannot deadlock while every CTA is resident.  Every wait is bounded
+// in time (about two seconds): one that gives up sets bit 1 of the workspace's
+// timeout word and the kernel's abort word (which the work-list kernel clears
+// before the launch), every other CTA polling a global flag sees the abort and
+// stops, and each CTA waits for its own copies in flight and frees its tensor
+// memory before it exits.
+#include <cudaTypedefs.h>
+#include <stdio.h>
+#include <stdlib.h>
+
+#include "kda_internal.cuh"
+#include "kda_tc_chunk.cuh"
+
+namespace kda {
+
+PFN_cuTensorMapEncodeTiled_v12000 tc_encode_fn();
+bool tc_make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elem, int H,
+                 long long T, int box_x, CUtensorMapSwizzle swz);
+
+namespace {
+
+using namespace tc;
+
+constexpr int kThreads = 320;
+
+// Consumer shared memory (from the same 1024-aligned base; the descriptor,
+// barrier and misc areas are those of the front map).
+constexpr uint32_t kStage = (uint32_t)kSplitStepBytes;   // one step block, 65 KB
+constexpr uint32_t C_V0 = 2 * kStage;                    // two v tiles, 16 KB each
+constexpr uint32_t C_OST = C_V0 + 32768;                 // O staging [64][128] bf16
+constexpr uint32_t kConsumerEnd = C_OST + 16384;
+static_assert(kBlkBytes <= kStage && kStage % 1024 == 0, "step block layout");
+static_assert(kConsumerEnd <= OFF_DESC, "consumer map overlaps the bookkeeping area");
+
+// A producer's job, written by its data-movement warp.
+struct JobDesc {
+    long long bos, eos;
+    int32_t u, c, h, npass;
+    int32_t terminate, pad;
+};
+constexpr uint32_t OFF_JOB = OFF_Y;        // 2 JobDesc (unused by the front phases)
+static_assert(OFF_JOB + 2 * sizeof(JobDesc) <= OFF_GL, "job area overflows");
+
+constexpr long long kPollTimeout = 1ll << 32;   // ~2 s of SM clock
+
+// Polls a global flag until pred(value) holds.  Returns false after about
+// kPollTimeout cycles (recording the timeout for the caller and the abort for
+// the other CTAs), or at once when another CTA has already given up.
+template <typename Pred>
+__device__ __forceinline__ bool poll_flag(const Ctx& X, const int32_t* flag, Pred pred,
+                                          int32_t* seen)
+{
+    const long long t0 = clock64();
+    for (int i = 0;; ++i) {
+        const int32_t v = ld_acquire_gpu(flag);
+        if (pred(v)) {
+            *seen = v;
+            return true;
+        }
+        if ((i & 31) == 31) {
+            if (ld_relaxed_gpu(X.ws_abort) != 0) return false;
+            if (clock64() - t0 > kPollTimeout) {
+                atomicOr(X.ws_err, 2);
+                atomicExch(X.ws_abort, 1);
+                return false;
+            }
+        }
+        __nanosleep(40);
+    }
+}
+
+__device__ __forceinline__ bool global_abort(const Ctx& X)
+{
+    return ld_relaxed_gpu(X.ws_abort) != 0;
+}
+
+// ------------------------------------------------------------- consumer
+template <typename TO>
+__device__ __forceinline__ void consumer(const Ctx& X, uint32_t tmem, int warp, int lane,
+                                         const CUtensorMap* tm_v, const CUtensorMap* tm_o,
+                                         const float* S0, const int32_t* cu, const int32_t* ws,
+                                         long long total_tokens, int H, TO* o, float* S_final,
+                                         int U, int R, int32_t* flags, const uint8_t* ring)
+{
+    uint8_t* sm = X.sm;
+    const int u = blockIdx.x;
+    const int rank = u / H, h = u % H;
+    long long bos = 0, eos = total_tokens;
+    int n = 0;
+    if (cu != nullptr) {
+        n = ws[kWsHeaderBytes / sizeof(int32_t) + rank];
+        bos = cu[n];
+        eos = cu[n + 1];
+    }
+    const int nch = (int)((eos - bos + kC - 1) / kC);
+    const long long sbase = ((long long)n * H + h) * kD * kD;
+    const int32_t* full = flags + (size_t)u * R;
+    int32_t* consumed = flags + (size_t)U * R + u;
+    const uint8_t* uring = ring + (size_t)u * R * 2 * kStage;
+
+    if (warp == 0) {
+        // ------------------------------------------------------ loader
+        if (lane != 0) return;
+        tma_prefetch_desc(tm_v);
+        int step = 0, issued_st[2] = {0, 0}, issued_v[2] = {0, 0};
+        bool ok = true;
+        for (int c = 0; c < nch && ok; ++c) {
+            const int slot = c % R;
+            int32_t val = 0;
+            ok = poll_flag(X, full + slot, [&](int32_t v) { return (v >> 1) == c + 1; }, &val);
+            if (!ok) break;
+            fence_proxy_async_global();        // the bulk copies below read what the producer wrote
+            const int npass = (val & 1) + 1;
+            const long long t0 = bos + (long long)c * kC;
+            const int len = (eos - t0 < kC) ? (int)(eos - t0) : kC;
+            for (int p = 0; p < npass; ++p) {
+                const int s = step & 1;
+                if (step >= 2 && !wait_bar(X, B_ST_EMPTY0 + s, (step - 2) >> 1)) { ok = false; break; }
+                StepDesc d;
+                d.t0 = (int32_t)t0;
+                d.len = len;
+                d.lo = (npass == 1) ? 0 : (p == 0 ? 0 : 32);
+                d.hi = (npass == 1) ? len : (p == 0 ? min(32, len) : len);
+                d.first_pass = (p == 0);
+                d.last_pass = (p == npass - 1);
+                d.last_step = (c == nch - 1) && (p == npass - 1);
+                d.chunk = c;
+                X.desc[s] = d;
+                mbar_arrive_expect_tx(&X.bar[B_ST_FULL0 + s], kBlkBytes);
+                bulk_load(sm + s * kStage, uring + ((size_t)slot * 2 + p) * kStage, kBlkBytes,
+                          &X.bar[B_ST_FULL0 + s]);
+                ++issued_st[s];
+                if (p == 0) {
+                    const int vb = c & 1;
+                    const int bf = vb ? B_V_FULL1 : B_V_FULL, be = vb ? B_V_EMPTY1 : B_V_EMPTY;
+                    if (c >= 2 && !wait_bar(X, be, (c - 2) >> 1)) { ok = false; break; }
+                    mbar_arrive_expect_tx(&X.bar[bf], 16384);
+                    tma_load_2d(sm + C_V0 + vb * 16384, tm_v, h * kD, (int32_t)t0, &X.bar[bf]);
+                    tma_load_2d(sm + C_V0 + vb * 16384 + 8192, tm_v, h * kD + 64, (int32_t)t0,
+                                &X.bar[bf]);
+                    ++issued_v[vb];
+                }
+                ++step;
+            }
+        }
+        if (!ok) {
+            // Stop the other warps and let the copies already issued land.
+            atomicExch(&X.misc->abort, 1);
+            for (int s = 0; s < 2; ++s) {
+                if (issued_st[s]) mbar_wait(&X.bar[B_ST_FULL0 + s], (issued_st[s] - 1) & 1, 1ll << 28);
+                if (issued_v[s])
+                    mbar_wait(&X.bar[s ? B_V_FULL1 : B_V_FULL], (issued_v[s] - 1) & 1, 1ll << 28);
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------- MMA
+        if (lane != 0 || nch == 0) return;
+        for (int step = 0;; ++step) {
+            if (!wait_bar(X, B_OPS, step)) break;
+            tc_fence_after();
+            const StepDesc d = X.desc[step & 1];
+            const uint32_t blk = smem_u32(sm + (step & 1) * kStage);
+            // The compute group saw this block land: the ring slot is free
+            // once the chunk's last block is here.
+            if (d.last_pass) st_relaxed_gpu(consumed, d.chunk + 1);
+            mma_back_c(tmem, blk + BLK_WT, blk + BLK_T16, smem_u32(sm + C_V0 + (d.chunk & 1) * 16384));
+            mma_commit(&X.bar[B_MMA_C]);
+            if (d.last_pass) mma_commit(&X.bar[(d.chunk & 1) ? B_V_EMPTY1 : B_V_EMPTY]);
+            if (!wait_bar(X, B_U, step)) break;
+            tc_fence_after();
+            mma_back_os(tmem, blk + BLK_P);
+            mma_commit(&X.bar[B_MMA_OS]);
+            mma_commit(&X.bar[B_ST_EMPTY0 + (step & 1)]);
+            if (d.last_step) break;
+        }
+    } else {
+        // ------------------------------------------------ compute group
+        const Lane t = make_lane(threadIdx.x - 64, warp, lane);
+        state_load(t, tmem, S0, sbase);
+        bool alive = nch > 0;
+        StepDesc prev;
+        prev.t0 = 0;
+        prev.lo = prev.hi = 0;
+        int step = 0;
+        // The O of a step is read from tensor memory before the next step's
+        // products start and stored while they run.
+        auto store_prev_o = [&](const uint32_t (&dd)[32]) {
+            const bool tma_out = (sizeof(TO) == 2) && prev.lo == 0 && prev.hi == kC;
+            o_store<TO>(t, dd, tma_out, tm_o, sm + C_OST, o, (long long)prev.t0, prev.lo, prev.hi,
+                        h, H);
+        };
+        while (alive) {
+            const int s = step & 1;
+            if (!group_wait(X, B_ST_FULL0 + s, step >> 1)) { alive = false; break; }
+            const StepDesc d = X.desc[s];
+            if (d.first_pass) {
+                const int vb = d.chunk & 1;
+                if (!group_wait(X, vb ? B_V_FULL1 : B_V_FULL, d.chunk >> 1)) { alive = false; break; }
+                v_tile_to_f16(sm + C_V0 + vb * 16384, t.ct);
+            }
+            uint32_t dd[32];
+            if (step > 0) {
+                if (!group_wait(X, B_MMA_OS, step - 1)) { alive = false; break; }
+                tc_fence_after();
+                o_load(t, tmem, dd);
+            } else {
+                tc_fence_after();
+            }
+            state_decay(t, tmem, reinterpret_cast<const float*>(sm + s * kStage + BLK_GL));
+            fence_proxy_async_smem();             // the converted v tile
+            tc_fence_before();
+            if (t.ct == 0) bulk_wait_group_read0();   // the O staging is free again
+            group_sync();
+            if (t.ct == 0) mbar_arrive(&X.bar[B_OPS]);
+            if (step > 0) store_prev_o(dd);
+            prev = d;
+            if (!group_wait(X, B_MMA_C, step)) { alive = false; break; }
+            tc_fence_after();
+            u_to_f16(t, tmem);
+            tc_fence_before();
+            group_sync();
+            if (t.ct == 0) mbar_arrive(&X.bar[B_U]);
+            ++step;
+            if (d.last_step) break;
+        }
+        if (alive && step > 0 && group_wait(X, B_MMA_OS, step - 1)) {
+            tc_fence_after();
+            uint32_t dd[32];
+            o_load(t, tmem, dd);
+            tc_fence_before();
+            if (t.ct == 0) bulk_wait_group_read0();
+            group_sync();
+            store_prev_o(dd);
+        }
+        if (t.ct == 0) bulk_wait_group0();               // the last O store has landed
+        if (S_final && !*reinterpret_cast<volatile int32_t*>(&X.misc->abort))
+            state_store(t, tmem, S_final, sbase);
+    }
+}
+
+// ------------------------------------------------------------- producer
+__device__ __forceinline__ void producer(const Ctx& X, uint32_t tmem, int warp, int lane,
+                                         const CUtensorMap* tm_q, const CUtensorMap* tm_k,
+                                         const CUtensorMap* tm_g, const float* beta,
+                                         const int32_t* cu, int32_t* ws, long long total_tokens,
+                                         int H, int U, int R, int32_t* flags, uint8_t* ring)
+{
+    uint8_t* sm = X.sm;
+    JobDesc* jd = reinterpret_cast<JobDesc*>(sm + OFF_JOB);
+    if (warp == 0) {
+        // ---------------------------------------------- data movement
+        if (lane == 0) {
+            tma_prefetch_desc(tm_q);
+            tma_prefetch_desc(tm_k);
+            tma_prefetch_desc(tm_g);
+        }
+        float* sBin = reinterpret_cast<float*>(sm + OFF_BIN);
+        const long long maxlen = (cu != nullptr) ? ws[kWsMaxLenWord] : total_tokens;
+        const long long total_jobs = (long long)U * ((maxlen + kC - 1) / kC);
+        unsigned long long* counter = reinterpret_cast<unsigned long long*>(ws + kWsJobWord);
+        const int32_t* order = ws + kWsHeaderBytes / sizeof(int32_t);
+        // Publishes job jc's slot once the compute group has written it.
+        auto publish = [&](int jc) -> bool {
+            if (!wait_bar(X, B_JOB_DONE, jc)) return false;
+            const JobDesc& j = jd[jc & 1];
+            fence_acq_rel_gpu();
+            st_release_gpu(flags + (size_t)j.u * R + j.c % R, 2 * (j.c + 1) + (j.npass - 1));
+            return true;
+        };
+        int jc = 0, issued = 0;
+        bool ok = true;
+        for (;; ++jc) {
+            if (jc > 0) {
+                if (lane == 0) ok = wait_bar(X, B_QKG_EMPTY, jc - 1);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) break;
+            }
+            long long bos = 0, eos = 0;
+            int uu = -1, c = 0, hh = 0;
+            if (lane == 0) {
+                for (;;) {
+                    const long long j = (long long)atomicAdd(counter, 1ull);
+                    if (j >= total_jobs || global_abort(X)) {
+                        uu = -1;
+                        break;
+                    }
+                    c = (int)(j / U);
+                    uu = (int)(j % U);
+                    hh = uu % H;
+                    const int nn = (cu != nullptr) ? order[uu / H] : 0;
+                    bos = (cu != nullptr) ? cu[nn] : 0;
+                    eos = (cu != nullptr) ? cu[nn + 1] : total_tokens;
+                    if ((long long)c * kC < eos - bos) break;   // else: this unit has no chunk c
+                }
+            }
+            uu = __shfl_sync(0xffffffffu, uu, 0);
+            if (uu < 0) {
+                if (lane == 0) {
+                    jd[jc & 1].terminate = 1;
+                    mbar_arrive(&X.bar[B_QKG_FULL]);       // wakes the compute group
+                }
+                break;
+            }
+            c = __shfl_sync(0xffffffffu, c, 0);
+            hh = __shfl_sync(0xffffffffu, hh, 0);
+            bos = __shfl_sync(0xffffffffu, bos, 0);
+            eos = __shfl_sync(0xffffffffu, eos, 0);
+            const long long t0 = bos + (long long)c * kC;
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int r = lane * 2 + j;
+                const long long tt = t0 + r;
+                sBin[r] = (tt < eos) ? beta[tt * H + hh] : 0.f;
+            }
+            __syncwarp();
+            if (lane == 0) {
+                JobDesc& j = jd[jc & 1];
+                j.bos = bos;
+                j.eos = eos;
+                j.u = uu;
+                j.c = c;
+                j.h = hh;
+                j.npass = 1;
+                j.terminate = 0;
+                mbar_arrive_expect_tx(&X.bar[B_QKG_FULL], 2 * 16384 + 32768);
+                tma_load_2d(sm + OFF_Q, tm_q, hh * kD, (int32_t)t0, &X.bar[B_QKG_FULL]);
+                tma_load_2d(sm + OFF_K, tm_k, hh * kD, (int32_t)t0, &X.bar[B_QKG_FULL]);
+                tma_load_2d(sm + OFF_G, tm_g, hh * kD, (int32_t)t0, &X.bar[B_QKG_FULL]);
+                ++issued;
+                if (jc > 0) ok = publish(jc - 1);
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+        }
+        if (lane == 0) {
+            if (ok && jc > 0) ok = publish(jc - 1);
+            // On abort, let the copies already issued land before the CTA exits.
+            if (!ok || X.misc->abort) {
+                atomicExch(&X.misc->abort, 1);
+                if (issued) mbar_wait(&X.bar[B_QKG_FULL], (issued - 1) & 1, 1ll << 28);
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------- MMA
+        if (lane != 0) return;
+        const FrontDescs D = make_front_descs(sm);
+        for (int step = 0;; ++step) {
+            if (!wait_bar(X, B_OPS, step)) break;
+            tc_fence_after();
+            if (X.desc[step & 1].last_step) break;     // no more jobs
+            if (!mma_front(X, tmem, D, step)) break;
+        }
+    } else {
+        // ------------------------------------------------ compute group
+        const Lane t = make_lane(threadIdx.x - 64, warp, lane);
+        const int ct = t.ct;
+        const int32_t* consumed = flags + (size_t)U * R;
+        int step = 0;
+        for (int jc = 0;; ++jc) {
+            if (!group_wait(X, B_QKG_FULL, jc)) break;
+            const JobDesc job = jd[jc & 1];
+            if (job.terminate) {
+                if (ct == 0) {
+                    X.desc[step & 1].last_step = 1;
+                    mbar_arrive(&X.bar[B_OPS]);        // lets the MMA warp finish
+                }
+                break;
+            }
+            const long long t0 = job.bos + (long long)job.c * kC;
+            const int len = (job.eos - t0 < kC) ? (int)(job.eos - t0) : kC;
+            uint8_t* slot = ring + ((size_t)job.u * R + job.c % R) * 2 * kStage;
+            // The slot is free once the consumer has copied out chunk c - R.
+            if (ct == 0 && job.c >= R) {
+                int32_t seen;
+                const int32_t want = job.c - R + 1;
+                if (!poll_flag(X, consumed + job.u, [&](int32_t v) { return v >= want; }, &seen))
+                    atomicExch(&X.misc->abort, 1);
+            }
+            float2 Gq[16];
+            PassParams pp;
+            const int npass = gate_prep(X, t, len, Gq, pp);   // (a group barrier inside)
+            if (*reinterpret_cast<volatile int32_t*>(&X.misc->abort)) break;
+            bool alive = true;
+            for (int p = 0; p < npass; ++p) {
+                const Pass ps = select_pass(pp, p, npass, len);
+                uint8_t* blk = slot + (size_t)p * kStage;
+                pass_factors(X, t, ps, reinterpret_cast<float*>(blk + BLK_GL));
+                if (ct == 0) X.desc[step & 1].last_step = 0;
+                group_sync();
+                gram_operands(X, t, ps, Gq, blk + BLK_QG, blk + BLK_KT);
+                fence_proxy_async_smem();
+                group_sync();
+                if (ct == 0) mbar_arrive(&X.bar[B_OPS]);
+                if (!gram_readout(X, t, tmem, ps.lo, ps.hi, step, blk + BLK_P)) { alive = false; break; }
+                if (!ut_solve(X, t, tmem, warp, step, p == npass - 1, blk + BLK_T16)) { alive = false; break; }
+                if (!w_readout(X, t, tmem, step, blk + BLK_WT)) { alive = false; break; }
+                ++step;
+            }
+            if (!alive) break;
+            // Every thread's operand stores precede this arrive (the group
+            // barrier at the end of w_readout); the data-movement warp
+            // publishes the slot.
+            if (ct == 0) {
+                jd[jc & 1].npass = npass;
+                mbar_arrive(&X.bar[B_JOB_DONE]);
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------- the kernel
+template <typename TO>
+__global__ void __launch_bounds__(kThreads, 1)
+prefill_split_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUtensorMap tm_v,
+                     const __grid_constant__ CUtensorMap tm_o, const float* __restrict__ beta,
+                     const float* S0, const int32_t* __restrict__ cu, int32_t* ws,
+                     long long total_tokens, int H, TO* __restrict__ o, float* S_final, int U, int R,
+                     int32_t* flags, uint8_t* ring)
+{
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    Ctx X;
+    X.sm = sm;
+    X.bar = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
+    X.desc = reinterpret_cast<StepDesc*>(sm + OFF_DESC);
+    X.misc = reinterpret_cast<Misc*>(sm + OFF_MISC);
+    X.ws_err = ws + kWsTimeoutWord;
+    X.ws_abort = ws + kWsAbortWord;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (cu != nullptr && ws[kWsErrorWord] != 0) return;   // uniform: every thread returns
+
+    if (tid == 0) {
+        for (int b = 0; b < kNumBars; ++b) mbar_init(&X.bar[b], 1);
+        X.misc->abort = 0;
+        X.misc->wide = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(&X.misc->tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = X.misc->tmem_base;
+
+    if ((int)blockIdx.x < U)
+        consumer<TO>(X, tmem, warp, lane, &tm_v, &tm_o, S0, cu, ws, total_tokens, H, o, S_final, U,
+                     R, flags, ring);
+    else
+        producer(X, tmem, warp, lane, &tm_q, &tm_k, &tm_g, beta, cu, ws, total_tokens, H, U, R,
+                 flags, ring);
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+template <typename TO>
+cudaError_t launch_typed(const void* q, const void* k, const void* v, const float* g,
+                         const float* beta, const float* S0, const int32_t* cu, int64_t T,
+                         int32_t H, void* o, float* S_final, int32_t* ws, const SplitPlan& plan,
+                         cudaStream_t stream)
+{
+    CUtensorMap mq, mk, mg, mv, mo;
+    const bool bf16_out = sizeof(TO) == 2;
+    if (!tc_make_map(&mq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, T, kD, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        (bf16_out && !tc_make_map(&mo, o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, T, kD,
+                                  CU_TENSOR_MAP_SWIZZLE_NONE)) ||
+        !tc_make_map(&mk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, T, kD, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !tc_make_map(&mg, g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, H, T, kD, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !tc_make_map(&mv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, T, 64, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    if (!bf16_out) mo = mq;
+    auto kern = prefill_split_kernel<TO>;
+    static bool attr_set = false;   // benign race: every writer stores the same value
+    if (!attr_set) {
+        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   (int)kSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    int per_sm = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const int grid = plan.units + plan.producers;
+    if (per_sm < 1 || grid > per_sm * device_sm_count()) return cudaErrorCooperativeLaunchTooLarge;
+
+    int32_t* flags = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(ws) + plan.flags_off);
+    uint8_t* ring = reinterpret_cast<uint8_t*>(ws) + plan.ring_off;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, mq, mk, mg, mv, mo, beta, S0, cu, ws, (long long)T, (int)H,
+                           static_cast<TO*>(o), S_final, (int)plan.units, (int)plan.ring, flags,
+                           ring);
+    if (e != cudaSuccess && debug_enabled())
+        fprintf(stderr, "kda: prefill_split launch failed: %s\n", cudaGetErrorString(e));
+    return e;
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_split(const void* q, const void* k, const void* v,
+                                 const float* log_alpha, const float* beta, const float* S0,
+                                 const int32_t* cu_seqlens, int32_t num_seqs,
+                                 int64_t total_tokens, int32_t H, kda_dtype_t dtype, void* o,
+                                 float* S_final, int32_t* ws, const SplitPlan& plan,
+                                 cudaStream_t stream)
+{
+    (void)num_seqs;
+    if (dtype == KDA_BF16_F32OUT)
+        return launch_typed<float>(q, k, v, log_alpha, beta, S0, cu_seqlens, total_tokens, H, o,
+                                   S_final, ws, plan, stream);
+    return launch_typed<__nv_bfloat16>(q, k, v, log_alpha, beta, S0, cu_seqlens, total_tokens, H,
+                                       o, S_final, ws, plan, stream);
+}
+
+}  // namespace kda

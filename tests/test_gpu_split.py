@@ -1,0 +1,145 @@
+"""GPU parity of the producer / consumer prefill (the path for batches with
+few (sequence, head) units).
+
+kda_prefill takes it when the units fill at most half of the SMs and the
+workspace has room for the operand ring (kda_prefill_workspace_bytes returns
+that size).  A workspace of only the base size selects the single-CTA kernel
+for the same call, so every case here runs both and checks
+
+  * each against the float64 oracle (the bf16 bound of the other parity
+    tests), and
+  * the two against each other: they evaluate the same products on the same
+    fp16 / bf16 operands in the same order, so o and S_final are equal bit
+    for bit;
+  * that the split kernel really ran (its job counter in the workspace) and
+    no wait gave up (the timeout word).
+"""
+import pytest
+import torch
+
+import synth
+from tests._parity import TOL, assert_close, compare_out, oracle_prefill, to64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def kda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import gated_delta_rule_05_gb300 as m
+    m.build()
+    m.lib()
+    return m
+
+
+def base_workspace_bytes(num_seqs):
+    """The work-list part of the workspace only (no ring)."""
+    return 256 + (num_seqs * 4 + 255) // 256 * 256
+
+
+def run_both(kda, inp, o_dtype=None):
+    d = inp.to("cuda")
+    N = len(inp.lengths)
+    T, H, dk = d.q.shape
+    need = kda.kda_prefill_workspace_bytes(N, H, dk, dk)
+    assert need > base_workspace_bytes(N), "shape should qualify for the split kernel"
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    o_s, S_s = kda.kda_prefill(d.q, d.k, d.v, d.log_alpha, d.beta, S0=d.S0,
+                               cu_seqlens=d.cu_seqlens, workspace=ws, o_dtype=o_dtype)
+    torch.cuda.synchronize()
+    words = ws[:24].view(torch.int32).cpu()
+    jobs = int(ws[16:24].view(torch.int64).item())
+    ws1 = torch.zeros(base_workspace_bytes(N), dtype=torch.uint8, device="cuda")
+    o_1, S_1 = kda.kda_prefill(d.q, d.k, d.v, d.log_alpha, d.beta, S0=d.S0,
+                               cu_seqlens=d.cu_seqlens, workspace=ws1, o_dtype=o_dtype)
+    torch.cuda.synchronize()
+    assert int(words[2]) == 0, "a device-side wait gave up"
+    assert int(ws[24:28].view(torch.int32).item()) == 0, "the split kernel aborted"
+    maxlen = max(inp.lengths)
+    assert int(words[3]) == maxlen
+    # every job was claimed (each producer also makes one failed claim)
+    assert jobs >= N * H * ((maxlen + 63) // 64)
+    return (o_s, S_s), (o_1, S_1)
+
+
+def check(kda, inp, o_dtype=None):
+    (o_s, S_s), (o_1, S_1) = run_both(kda, inp, o_dtype=o_dtype)
+    o_ref, S_ref = oracle_prefill(inp)
+    compare_out(o_s, o_ref, TOL["bf16"], "o (split)")
+    assert_close(to64(S_s), S_ref, TOL["bf16"], "S_final (split)")
+    assert torch.equal(o_s, o_1), "split and single-CTA outputs differ"
+    assert torch.equal(S_s, S_1), "split and single-CTA states differ"
+
+
+CASES = {
+    "one_seq_ragged": ([1000], 3),
+    "varlen_empty_ragged": ([0, 300, 0, 130, 64, 1, 65], 2),
+    "one_unit_long": ([5000], 1),
+    "many_chunks_few_units": ([20000], 4),
+}
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_split_matches_single_cta_and_oracle(kda, name):
+    lengths, H = CASES[name]
+    inp = synth.generate(lengths, H, 128, 128, dtype="bf16", s0_std=0.05, seed=600 + len(name))
+    check(kda, inp)
+
+
+def test_split_fp32_output(kda):
+    inp = synth.generate([700, 129], 3, 128, 128, dtype="bf16", s0_std=0.05, seed=611)
+    check(kda, inp, o_dtype=torch.float32)
+
+
+def test_split_wide_chunks_mixed(kda):
+    # Stretches of log_alpha = -5 (the lower bound) make some chunks' decay
+    # span too wide for one pass; they are processed as two 32-row steps while
+    # their neighbours take one.
+    inp = synth.generate([900, 333], 2, 128, 128, dtype="bf16", s0_std=0.05, seed=612)
+    g = inp.log_alpha
+    for a, b in ((40, 200), (450, 470), (700, 900), (1000, 1100)):
+        g[a:b] = -5.0
+    check(kda, inp)
+
+
+def test_split_all_wide(kda):
+    inp = synth.generate([640, 77], 2, 128, 128, dtype="bf16", s0_std=0.05, seed=613,
+                         gate_shift=-5.0)
+    check(kda, inp)
+
+
+def test_split_back_to_back_reuses_workspace(kda):
+    # Two calls on one workspace: the work-list kernel clears the hand-over
+    # flags and counters in between.
+    inp = synth.generate([400, 250], 2, 128, 128, dtype="bf16", s0_std=0.05, seed=614)
+    d = inp.to("cuda")
+    N, H = 2, 2
+    ws = torch.zeros(kda.kda_prefill_workspace_bytes(N, H, 128, 128), dtype=torch.uint8,
+                     device="cuda")
+    outs = []
+    for _ in range(2):
+        o, S = kda.kda_prefill(d.q, d.k, d.v, d.log_alpha, d.beta, S0=d.S0,
+                               cu_seqlens=d.cu_seqlens, workspace=ws)
+        torch.cuda.synchronize()
+        outs.append((o.clone(), S.clone()))
+    assert torch.equal(outs[0][0], outs[1][0])
+    assert torch.equal(outs[0][1], outs[1][1])
+    assert int(ws[8:12].view(torch.int32).item()) == 0
+
+
+def test_split_ignores_workspace_contents(kda):
+    # The workspace may hold anything on entry (the binding passes torch.empty);
+    # in particular the caller-owned timeout word may already have bit 1 set.
+    inp = synth.generate([3000], 4, 128, 128, dtype="bf16", s0_std=0.05, seed=615)
+    d = inp.to("cuda")
+    need = kda.kda_prefill_workspace_bytes(1, 4, 128, 128)
+    ws = torch.full((need,), 0xFF, dtype=torch.uint8, device="cuda")
+    o, S = kda.kda_prefill(d.q, d.k, d.v, d.log_alpha, d.beta, S0=d.S0, workspace=ws)
+    torch.cuda.synchronize()
+    assert int(ws[24:28].view(torch.int32).item()) == 0, "the split kernel aborted"
+    ws1 = torch.zeros(base_workspace_bytes(1), dtype=torch.uint8, device="cuda")
+    o1, S1 = kda.kda_prefill(d.q, d.k, d.v, d.log_alpha, d.beta, S0=d.S0, workspace=ws1)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o1)
+    assert torch.equal(S, S1)
