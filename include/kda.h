@@ -60,10 +60,13 @@ typedef enum {
     KDA_BF16_F32OUT = 2        /* q, k, v are bfloat16, o is float32 */
 } kda_dtype_t;
 
-/* Bytes of device workspace kda_prefill needs for num_seqs sequences
- * (the varlen work list: sequences ordered longest first, a work counter and
- * an error word).  Returns 0 when num_seqs < 1.  H, d_k and d_v are accepted
- * for forward compatibility and do not change the result today. */
+/* Bytes of device workspace kda_prefill needs for num_seqs sequences of H
+ * heads.  The workspace always holds the varlen work list (sequences ordered
+ * longest first, counters, an error word).  When d_k = d_v = 128 and the
+ * num_seqs x H (sequence, head) units fill at most half of the current
+ * device's SMs, the value also covers the operand ring of the producer /
+ * consumer prefill kernel (tens of MB at most; the size depends on the SM
+ * count).  Returns 0 when num_seqs < 1. */
 size_t kda_prefill_workspace_bytes(int32_t num_seqs, int32_t H, int32_t d_k,
                                    int32_t d_v);
 
@@ -88,9 +91,14 @@ size_t kda_prefill_workspace_bytes(int32_t num_seqs, int32_t H, int32_t d_k,
  *   S_final       [N, H, d_k, d_v] fp32, or NULL when not wanted.  May alias
  *                 S0 exactly (in-place resume); any other overlap is an error
  *                 the library cannot detect.
- *   workspace     device buffer of at least kda_prefill_workspace_bytes(...)
- *                 bytes, 256-byte aligned; its contents are overwritten.  It
- *                 must not be shared by calls that may run concurrently.
+ *   workspace     device buffer of at least 256 + 256 * ceil(N / 64) bytes
+ *                 (the work list), 256-byte aligned; its contents on entry do
+ *                 not matter and are overwritten.  It must not be shared by
+ *                 calls that may run concurrently.  A workspace of
+ *                 kda_prefill_workspace_bytes(...) bytes lets the call use the
+ *                 producer / consumer kernel where it applies (see Paths); a
+ *                 smaller one selects the single-CTA kernel, with the same
+ *                 results.
  *
  * If cu_seqlens violates its contract the kernels write nothing and set the
  * 32-bit word at byte offset 4 of the workspace to a nonzero value (it is
@@ -102,10 +110,15 @@ size_t kda_prefill_workspace_bytes(int32_t num_seqs, int32_t H, int32_t d_k,
  * reading them needs a synchronisation by the caller.
  *
  * Paths: bf16 inputs with d_k = d_v = 128 run on the tensor cores (tcgen05,
- * chunks of 64 tokens); every other supported shape, and every call made
- * while the environment variable KDA_FORCE_SIMT is set, runs the fp32
- * CUDA-core path (chunks of 16 tokens).  Both compute the same result up to
- * rounding.
+ * chunks of 64 tokens).  With few (sequence, head) units (at most half the
+ * SM count) and a full-size workspace, one cooperative launch of one CTA per
+ * SM splits each chunk's work: producer CTAs compute the parts that do not
+ * depend on the state and hand them, through the workspace, to one consumer
+ * CTA per unit that carries the state; otherwise one CTA per unit does both.
+ * Every other supported shape, and every call made while the environment
+ * variable KDA_FORCE_SIMT is set, runs the fp32 CUDA-core path (chunks of 16
+ * tokens).  All paths compute the same result up to rounding (the two
+ * tensor-core kernels bit for bit).
  */
 kda_status_t kda_prefill(const void *q, const void *k, const void *v,
                          const float *log_alpha, const float *beta,

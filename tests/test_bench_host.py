@@ -12,9 +12,13 @@ def test_helpers_exist_and_run():
     assert bench.BYTES_PER_TOKEN_HEAD == 768 + 512 + 4 + 256
     assert bench.FLOPS_PER_TOKEN_HEAD == 180224
     assert bench.decode_bytes_per_unit(128) == 2 * 65536 + 768 + 512 + 4 + 256
-    assert bench.committed_traffic("no/such_kernel", bench.PREFILL_SOURCES) is None
-    for f in bench.PREFILL_SOURCES + bench.DECODE_SOURCES:
+    srcs = [f for fs in bench.PREFILL_KERNELS.values() for f in fs]
+    assert bench.committed_traffic("no/such_kernel", srcs) is None
+    for f in srcs + bench.DECODE_SOURCES:
         assert bench.kernel_source_sha([f])
+    # a workspace larger than the work list means the split kernel runs
+    assert bench.prefill_kernel_name(512, 1) == "prefill_tc_kernel"
+    assert bench.prefill_kernel_name(40 << 20, 1) == "prefill_split_kernel"
 
 
 def test_clock_summary_parses_nvidia_smi_lines():
