@@ -61,8 +61,10 @@ constexpr int kThreads = 320;
 // Consumer shared memory (from the same 1024-aligned base; the descriptor,
 // barrier and misc areas are those of the front map).
 constexpr uint32_t kStage = (uint32_t)kSplitStepBytes;   // one step block, 65 KB
-constexpr uint32_t C_V0 = 2 * kStage;                    // two v tiles, 16 KB each
-constexpr uint32_t C_OST = C_V0 + 32768;                 // O staging [64][128] bf16
+constexpr uint32_t C_V0 = 2 * kStage;                    // four v tiles, 16 KB each
+constexpr int kVBufs = 4;
+constexpr int kVAhead = 2;                               // v tiles are loaded 2 chunks ahead
+constexpr uint32_t C_OST = C_V0 + kVBufs * 16384;        // O staging [64][128] bf16
 constexpr uint32_t kConsumerEnd = C_OST + 16384;
 static_assert(kBlkBytes <= kStage && kStage % 1024 == 0, "step block layout");
 static_assert(kConsumerEnd <= OFF_DESC, "consumer map overlaps the bookkeeping area");
@@ -75,6 +77,19 @@ struct JobDesc {
 };
 constexpr uint32_t OFF_JOB = OFF_Y;        // 2 JobDesc (unused by the front phases)
 static_assert(OFF_JOB + 2 * sizeof(JobDesc) <= OFF_GL, "job area overflows");
+// Producer-only uses of space that only the single-CTA kernel's back phases
+// need.  The g tile lives apart from the Gram lo parts and solve tiles (which
+// reuse OFF_G), so that the next job's q / k / g load can start as soon as
+// pass B is done.  (e^G Q)^T, Ktil^T, P and T are staged in shared memory and
+// sent to the ring with bulk copies: written straight from registers, each
+// warp store of the swizzled tiles would touch 32 different lines.
+constexpr uint32_t P_G = OFF_WT;          // g tile [64][128] fp32
+constexpr uint32_t P_QG = OFF_V;          // (e^G Q)^T staging, 16 KB
+constexpr uint32_t P_KT = OFF_KT;         // Ktil^T staging, 16 KB
+constexpr uint32_t P_P = OFF_P;           // P staging, 8 KB
+constexpr uint32_t P_T16 = OFF_T16;       // T staging, 8 KB (the decay stats' space)
+static_assert(P_G + 32768 <= P_P && P_P + 8192 <= P_KT && P_KT + 16384 <= OFF_A32,
+              "producer staging overlaps");
 
 constexpr long long kPollTimeout = 1ll << 32;   // ~2 s of SM clock
 
@@ -137,9 +152,23 @@ __device__ __forceinline__ void consumer(const Ctx& X, uint32_t tmem, int warp, 
         // ------------------------------------------------------ loader
         if (lane != 0) return;
         tma_prefetch_desc(tm_v);
-        int step = 0, issued_st[2] = {0, 0}, issued_v[2] = {0, 0};
+        int step = 0, issued_st[2] = {0, 0}, issued_v[kVBufs] = {0, 0, 0, 0};
         bool ok = true;
+        // v tile of chunk cv into buffer cv % 4, once chunk cv - 4 has left it.
+        auto issue_v = [&](int cv) -> bool {
+            const int vb = cv & (kVBufs - 1);
+            if (cv >= kVBufs && !wait_bar(X, B_SV_EMPTY0 + vb, (cv - kVBufs) / kVBufs)) return false;
+            const long long tv = bos + (long long)cv * kC;
+            mbar_arrive_expect_tx(&X.bar[B_SV_FULL0 + vb], 16384);
+            tma_load_2d(sm + C_V0 + vb * 16384, tm_v, h * kD, (int32_t)tv, &X.bar[B_SV_FULL0 + vb]);
+            tma_load_2d(sm + C_V0 + vb * 16384 + 8192, tm_v, h * kD + 64, (int32_t)tv,
+                        &X.bar[B_SV_FULL0 + vb]);
+            ++issued_v[vb];
+            return true;
+        };
+        for (int cv = 0; cv < kVAhead && cv < nch; ++cv) issue_v(cv);
         for (int c = 0; c < nch && ok; ++c) {
+            if (c + kVAhead < nch && !issue_v(c + kVAhead)) { ok = false; break; }
             const int slot = c % R;
             int32_t val = 0;
             ok = poll_flag(X, full + slot, [&](int32_t v) { return (v >> 1) == c + 1; }, &val);
@@ -165,43 +194,34 @@ __device__ __forceinline__ void consumer(const Ctx& X, uint32_t tmem, int warp, 
                 bulk_load(sm + s * kStage, uring + ((size_t)slot * 2 + p) * kStage, kBlkBytes,
                           &X.bar[B_ST_FULL0 + s]);
                 ++issued_st[s];
-                if (p == 0) {
-                    const int vb = c & 1;
-                    const int bf = vb ? B_V_FULL1 : B_V_FULL, be = vb ? B_V_EMPTY1 : B_V_EMPTY;
-                    if (c >= 2 && !wait_bar(X, be, (c - 2) >> 1)) { ok = false; break; }
-                    mbar_arrive_expect_tx(&X.bar[bf], 16384);
-                    tma_load_2d(sm + C_V0 + vb * 16384, tm_v, h * kD, (int32_t)t0, &X.bar[bf]);
-                    tma_load_2d(sm + C_V0 + vb * 16384 + 8192, tm_v, h * kD + 64, (int32_t)t0,
-                                &X.bar[bf]);
-                    ++issued_v[vb];
-                }
                 ++step;
             }
         }
         if (!ok) {
             // Stop the other warps and let the copies already issued land.
             atomicExch(&X.misc->abort, 1);
-            for (int s = 0; s < 2; ++s) {
+            for (int s = 0; s < 2; ++s)
                 if (issued_st[s]) mbar_wait(&X.bar[B_ST_FULL0 + s], (issued_st[s] - 1) & 1, 1ll << 28);
-                if (issued_v[s])
-                    mbar_wait(&X.bar[s ? B_V_FULL1 : B_V_FULL], (issued_v[s] - 1) & 1, 1ll << 28);
-            }
+            for (int vb = 0; vb < kVBufs; ++vb)
+                if (issued_v[vb]) mbar_wait(&X.bar[B_SV_FULL0 + vb], (issued_v[vb] - 1) & 1, 1ll << 28);
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA
-        if (lane != 0 || nch == 0) return;
+        // The whole warp runs this loop; the issue helpers elect one lane.
+        if (nch == 0) return;
         for (int step = 0;; ++step) {
-            if (!wait_bar(X, B_OPS, step)) break;
+            if (!warp_wait(X, B_OPS, step)) break;
             tc_fence_after();
             const StepDesc d = X.desc[step & 1];
             const uint32_t blk = smem_u32(sm + (step & 1) * kStage);
+            const int vb = d.chunk & (kVBufs - 1);
             // The compute group saw this block land: the ring slot is free
             // once the chunk's last block is here.
-            if (d.last_pass) st_relaxed_gpu(consumed, d.chunk + 1);
-            mma_back_c(tmem, blk + BLK_WT, blk + BLK_T16, smem_u32(sm + C_V0 + (d.chunk & 1) * 16384));
+            if (d.last_pass && lane == 0) st_relaxed_gpu(consumed, d.chunk + 1);
+            mma_back_c(tmem, blk + BLK_WT, blk + BLK_T16, smem_u32(sm + C_V0 + vb * 16384));
             mma_commit(&X.bar[B_MMA_C]);
-            if (d.last_pass) mma_commit(&X.bar[(d.chunk & 1) ? B_V_EMPTY1 : B_V_EMPTY]);
-            if (!wait_bar(X, B_U, step)) break;
+            if (d.last_pass) mma_commit(&X.bar[B_SV_EMPTY0 + vb]);
+            if (!warp_wait(X, B_U, step)) break;
             tc_fence_after();
             mma_back_os(tmem, blk + BLK_P);
             mma_commit(&X.bar[B_MMA_OS]);
@@ -229,8 +249,8 @@ __device__ __forceinline__ void consumer(const Ctx& X, uint32_t tmem, int warp, 
             if (!group_wait(X, B_ST_FULL0 + s, step >> 1)) { alive = false; break; }
             const StepDesc d = X.desc[s];
             if (d.first_pass) {
-                const int vb = d.chunk & 1;
-                if (!group_wait(X, vb ? B_V_FULL1 : B_V_FULL, d.chunk >> 1)) { alive = false; break; }
+                const int vb = d.chunk & (kVBufs - 1);
+                if (!group_wait(X, B_SV_FULL0 + vb, d.chunk / kVBufs)) { alive = false; break; }
                 v_tile_to_f16(sm + C_V0 + vb * 16384, t.ct);
             }
             uint32_t dd[32];
@@ -360,7 +380,7 @@ __device__ __forceinline__ void producer(const Ctx& X, uint32_t tmem, int warp, 
                 mbar_arrive_expect_tx(&X.bar[B_QKG_FULL], 2 * 16384 + 32768);
                 tma_load_2d(sm + OFF_Q, tm_q, hh * kD, (int32_t)t0, &X.bar[B_QKG_FULL]);
                 tma_load_2d(sm + OFF_K, tm_k, hh * kD, (int32_t)t0, &X.bar[B_QKG_FULL]);
-                tma_load_2d(sm + OFF_G, tm_g, hh * kD, (int32_t)t0, &X.bar[B_QKG_FULL]);
+                tma_load_2d(sm + P_G, tm_g, hh * kD, (int32_t)t0, &X.bar[B_QKG_FULL]);
                 ++issued;
                 if (jc > 0) ok = publish(jc - 1);
             }
@@ -377,10 +397,10 @@ __device__ __forceinline__ void producer(const Ctx& X, uint32_t tmem, int warp, 
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA
-        if (lane != 0) return;
+        // The whole warp runs this loop; the issue helpers elect one lane.
         const FrontDescs D = make_front_descs(sm);
         for (int step = 0;; ++step) {
-            if (!wait_bar(X, B_OPS, step)) break;
+            if (!warp_wait(X, B_OPS, step)) break;
             tc_fence_after();
             if (X.desc[step & 1].last_step) break;     // no more jobs
             if (!mma_front(X, tmem, D, step)) break;
@@ -392,6 +412,9 @@ __device__ __forceinline__ void producer(const Ctx& X, uint32_t tmem, int warp, 
         const int32_t* consumed = flags + (size_t)U * R;
         int step = 0;
         for (int jc = 0;; ++jc) {
+            // The previous job's T copy has read its staging area (the decay
+            // stats go there) before the group passes the barrier below.
+            if (ct == 0) bulk_wait_group_read0();
             if (!group_wait(X, B_QKG_FULL, jc)) break;
             const JobDesc job = jd[jc & 1];
             if (job.terminate) {
@@ -413,29 +436,50 @@ __device__ __forceinline__ void producer(const Ctx& X, uint32_t tmem, int warp, 
             }
             float2 Gq[16];
             PassParams pp;
-            const int npass = gate_prep(X, t, len, Gq, pp);   // (a group barrier inside)
+            const int npass = gate_prep(X, t, len, reinterpret_cast<const float*>(sm + P_G), Gq, pp);
             if (*reinterpret_cast<volatile int32_t*>(&X.misc->abort)) break;
             bool alive = true;
             for (int p = 0; p < npass; ++p) {
                 const Pass ps = select_pass(pp, p, npass, len);
                 uint8_t* blk = slot + (size_t)p * kStage;
                 pass_factors(X, t, ps, reinterpret_cast<float*>(blk + BLK_GL));
-                if (ct == 0) X.desc[step & 1].last_step = 0;
+                if (ct == 0) {
+                    X.desc[step & 1].last_step = 0;
+                    bulk_wait_group_read0();       // staging areas free again
+                }
                 group_sync();
-                gram_operands(X, t, ps, Gq, blk + BLK_QG, blk + BLK_KT);
+                gram_operands(X, t, ps, Gq, sm + P_QG, sm + P_KT);
                 fence_proxy_async_smem();
                 group_sync();
-                if (ct == 0) mbar_arrive(&X.bar[B_OPS]);
-                if (!gram_readout(X, t, tmem, ps.lo, ps.hi, step, blk + BLK_P)) { alive = false; break; }
-                if (!ut_solve(X, t, tmem, warp, step, p == npass - 1, blk + BLK_T16)) { alive = false; break; }
+                if (ct == 0) {
+                    mbar_arrive(&X.bar[B_OPS]);
+                    // q, k, g and beta are read: the next job may load.
+                    if (p == npass - 1) mbar_arrive(&X.bar[B_QKG_EMPTY]);
+                    bulk_store(blk + BLK_QG, sm + P_QG, 16384);
+                    bulk_store(blk + BLK_KT, sm + P_KT, 16384);
+                    bulk_commit_group();
+                }
+                if (!gram_readout(X, t, tmem, ps.lo, ps.hi, step, sm + P_P)) { alive = false; break; }
+                if (ct == 0) {
+                    bulk_store(blk + BLK_P, sm + P_P, 8192);
+                    bulk_commit_group();
+                }
+                if (!ut_solve(X, t, tmem, warp, step, false, sm + P_T16)) { alive = false; break; }
+                if (ct == 0) {
+                    bulk_store(blk + BLK_T16, sm + P_T16, 8192);
+                    bulk_commit_group();
+                }
                 if (!w_readout(X, t, tmem, step, blk + BLK_WT)) { alive = false; break; }
                 ++step;
             }
             if (!alive) break;
-            // Every thread's operand stores precede this arrive (the group
-            // barrier at the end of w_readout); the data-movement warp
-            // publishes the slot.
+            // Every thread's direct stores (-W^T, e^{G_last}) precede this
+            // point (the group barrier at the end of w_readout), and ct 0's
+            // bulk copies have completed; the data-movement warp publishes
+            // the slot.
             if (ct == 0) {
+                bulk_wait_group0();
+                fence_proxy_async_global();
                 jd[jc & 1].npass = npass;
                 mbar_arrive(&X.bar[B_JOB_DONE]);
             }

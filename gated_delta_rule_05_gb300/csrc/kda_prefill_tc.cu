@@ -18,7 +18,7 @@
 //
 // CTA roles (320 threads):
 //   warp 0      TMA: q, k, g tiles (64 x 128) and the v tile, beta by plain loads
-//   warp 1      one thread issues every tcgen05.mma and commit
+//   warp 1      issues every tcgen05.mma and commit (warp-wide, one elected lane)
 //   warps 2..9  the compute group (256 threads) runs every CUDA-core phase of a
 //               chunk together: gate prep, state decay, Gram readout, the UT
 //               solve's diagonal blocks, and every TMEM readout.  The chunk's
@@ -180,20 +180,21 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA
-        if (lane == 0 && nch > 0) {
+        // The whole warp runs this loop; the issue helpers elect one lane.
+        if (nch > 0) {
             const FrontDescs D = make_front_descs(sm);
             for (int step = 0;; ++step) {
-                if (!wait_bar(X, B_OPS, step)) break;
+                if (!warp_wait(X, B_OPS, step)) break;
                 tc_fence_after();
                 const StepDesc d = X.desc[step & 1];
                 if (!mma_front(X, tmem, D, step)) break;
-                if (!wait_bar(X, B_CV, step)) break;   // -W^T, S^T copy, v tile ready
+                if (!warp_wait(X, B_CV, step)) break;   // -W^T, S^T copy, v tile ready
                 tc_fence_after();
                 // The U^T P^T term of O^T follows once U^T is ready.
                 mma_back_c(tmem, smem_u32(sm + OFF_WT), smem_u32(sm + OFF_T16), smem_u32(sm + OFF_V));
                 mma_commit(&X.bar[B_MMA_C]);
                 if (d.last_pass) mma_commit(&X.bar[B_V_EMPTY]);
-                if (!wait_bar(X, B_U, step)) break;
+                if (!warp_wait(X, B_U, step)) break;
                 tc_fence_after();
                 mma_back_os(tmem, smem_u32(sm + OFF_P));
                 mma_commit(&X.bar[B_MMA_OS]);
@@ -214,7 +215,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             if (!group_wait(X, B_QKG_FULL, ch)) break;
             float2 Gq[16];
             PassParams pp;
-            const int npass = gate_prep(X, t, len, Gq, pp);
+            const int npass = gate_prep(X, t, len, reinterpret_cast<const float*>(sm + OFF_G), Gq, pp);
             for (int p = 0; p < npass; ++p) {
                 const Pass ps = select_pass(pp, p, npass, len);
                 pass_factors(X, t, ps, reinterpret_cast<float*>(sm + OFF_GL));

@@ -130,6 +130,16 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int32_t x, 
         : "memory");
 }
 
+// Plain (untiled) bulk copy shared -> global, tracked by the issuing
+// thread's bulk group.  Both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_store(void* dst, const void* src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                     reinterpret_cast<uint64_t>(dst)),
+                 "r"(smem_u32(src)), "r"(bytes)
+                 : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit_group()
 {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
@@ -339,34 +349,46 @@ __host__ __device__ constexpr uint32_t make_idesc_f16(uint32_t M, uint32_t N, bo
            ((b_mn_major ? 1u : 0u) << 16) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
-// D (TMEM) = / += A (smem descriptor) x B (smem descriptor).  One thread.
+// The MMA issue helpers below are executed by all 32 threads of a converged
+// warp: elect.sync picks one lane, which issues the instruction.  Keeping the
+// whole warp on the issuing path lets the compiler hold the descriptors in
+// uniform registers, which makes back-to-back issue markedly cheaper than
+// issuing from a single-lane branch.
+
+// D (TMEM) = / += A (smem descriptor) x B (smem descriptor).
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                        uint32_t idesc, uint32_t accumulate)
 {
     asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "{\n\t.reg .pred p, e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
-// D (TMEM) = / += A (TMEM) x B (smem descriptor).  One thread.
+// D (TMEM) = / += A (TMEM) x B (smem descriptor).
 __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
                                        uint32_t idesc, uint32_t accumulate)
 {
     asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "{\n\t.reg .pred p, e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
         "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
-// Arrive once on `bar` when every tcgen05.mma issued so far by this thread
-// has completed.
+// Arrive once on `bar` when every tcgen05.mma issued so far by the warp's
+// elected lane has completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar)
 {
     asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
             smem_u32(bar))
         : "memory");
 }

@@ -96,8 +96,8 @@ constexpr uint32_t OFF_BIN = 226304;   // beta of the loaded chunk
 constexpr uint32_t OFF_BST = 226560;   // beta of the current pass (masked)
 constexpr uint32_t OFF_DESC = 226816;  // 2 step descriptors
 constexpr uint32_t OFF_BAR = 226880;   // mbarriers (kNumBars x 8 B)
-constexpr uint32_t OFF_MISC = 227104;  // tmem base, flags
-constexpr uint32_t kSmemUsed = 227120;
+constexpr uint32_t OFF_MISC = 227152;  // tmem base, flags
+constexpr uint32_t kSmemUsed = 227168;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;   // + alignment slack
 constexpr int LDA = 68;                // row stride (floats) of A / X: 16-byte aligned rows
 
@@ -117,7 +117,8 @@ enum Bar {
     B_CV, B_MMA_C, B_U, B_MMA_OS,
     B_S1, B_R1, B_S2, B_R2, B_S3, B_R3, B_S4, B_R4,   // UT solve rounds
     B_JOB_DONE,                                        // split producer: operands written
-    B_V_FULL1, B_V_EMPTY1,                             // split consumer: second buffers
+    B_SV_FULL0, B_SV_FULL1, B_SV_FULL2, B_SV_FULL3,    // split consumer: v tile buffers
+    B_SV_EMPTY0, B_SV_EMPTY1, B_SV_EMPTY2, B_SV_EMPTY3,
     B_ST_FULL0, B_ST_FULL1, B_ST_EMPTY0, B_ST_EMPTY1,  // split consumer: operand stages
     kNumBars
 };
@@ -203,6 +204,17 @@ __device__ __forceinline__ bool group_wait(const Ctx& X, int b, uint32_t phase)
 
 __device__ __forceinline__ void group_sync() { named_bar_sync(kGroupBar, kGroup); }
 
+// The MMA warp runs its loop with all 32 lanes (the issue helpers elect one
+// lane).  Every lane waits on the barrier itself and the lanes then agree on
+// the outcome, so the warp never diverges: a warp whose lane 0 polls while
+// the other lanes wait for it at a warp-synchronous instruction was measured
+// to slow the whole kernel down by half.
+__device__ __forceinline__ bool warp_wait(const Ctx& X, int b, uint32_t phase)
+{
+    const bool ok = wait_bar(X, b, phase);
+    return __all_sync(0xffffffffu, ok) != 0;
+}
+
 // 16 x 16 unit-lower diagonal block inverse, column j (j < 16) of block b by
 // forward substitution; x[r] for r < j is 0 and x[j] is 1.
 __device__ __forceinline__ void diag_block_column(const float* sA, int b, int j, float (&x)[16])
@@ -265,14 +277,14 @@ struct Pass {
 };
 
 // ---------------------------------------------------------------------------
-// Front phase 1: decay scan of this thread's 16 rows x 2 channels (log2
-// units, relative to the start of its row quarter, kept in Gq), the two-pass
-// vote and both pass layouts' factors.  Returns the number of passes (1, 2).
-__device__ __forceinline__ int gate_prep(const Ctx& X, const Lane& t, int len, float2 (&Gq)[16],
-                                         PassParams& pp)
+// Front phase 1: decay scan of this thread's 16 rows x 2 channels of the g
+// tile sG ([64][128] fp32; log2 units, relative to the start of its row
+// quarter, kept in Gq), the two-pass vote and both pass layouts' factors.
+// Returns the number of passes (1, 2).
+__device__ __forceinline__ int gate_prep(const Ctx& X, const Lane& t, int len, const float* sG,
+                                         float2 (&Gq)[16], PassParams& pp)
 {
     const int cp = t.cp, rq = t.rq;
-    const float* sG = reinterpret_cast<const float*>(X.sm + OFF_G);
     float* sStat = reinterpret_cast<float*>(X.sm + OFF_STAT);   // [3][4][128]
     {
         float2 G = make_float2(0.f, 0.f), mx = G, mn = G;
@@ -500,6 +512,7 @@ __device__ __forceinline__ bool gram_readout(const Ctx& X, const Lane& t, uint32
             }
         }
     }
+    fence_proxy_async_smem();      // P may be copied out by the async proxy
     tc_fence_before();
     group_sync();
     return true;
@@ -840,7 +853,8 @@ __device__ __forceinline__ FrontDescs make_front_descs(uint8_t* sm)
 }
 
 // The front products of one step, after B_OPS: the Gram, the four solve
-// rounds and W^T.  Returns false if a wait gave up.
+// rounds and W^T.  Called by the whole MMA warp.  Returns false if a wait
+// gave up.
 __device__ __forceinline__ bool mma_front(const Ctx& X, uint32_t tmem, const FrontDescs& D,
                                           int step)
 {
@@ -852,18 +866,18 @@ __device__ __forceinline__ bool mma_front(const Ctx& X, uint32_t tmem, const Fro
     for (int s = 0; s < 8; ++s) mma_ss(tmem + TM_G, D.ADLO + 128 * s, D.BDHL + 128 * s, D.id_g, 1);
     mma_commit(&X.bar[B_MMA_G]);
     // UT solve: N = D A_off ; N^2 = N N ; Y = I D' + N^2 D' ; T = Y - N Y.
-    if (!wait_bar(X, B_S1, step)) return false;
+    if (!warp_wait(X, B_S1, step)) return false;
     tc_fence_after();
 #pragma unroll
     for (int s = 0; s < 4; ++s) mma_ss(tmem + TM_N, D.DM + 128 * s, D.AO + 128 * s, D.id_r1, s > 0);
     mma_commit(&X.bar[B_R1]);
-    if (!wait_bar(X, B_S2, step)) return false;
+    if (!warp_wait(X, B_S2, step)) return false;
     tc_fence_after();
 #pragma unroll
     for (int s = 0; s < 4; ++s)
         mma_ts(tmem + TM_N2, tmem + TM_NA + 8 * s, D.NB + 128 * s, D.id_mn, s > 0);
     mma_commit(&X.bar[B_R2]);
-    if (!wait_bar(X, B_S3, step)) return false;
+    if (!warp_wait(X, B_S3, step)) return false;
     tc_fence_after();
 #pragma unroll
     for (int s = 0; s < 4; ++s)
@@ -871,13 +885,13 @@ __device__ __forceinline__ bool mma_front(const Ctx& X, uint32_t tmem, const Fro
 #pragma unroll
     for (int s = 0; s < 4; ++s) mma_ts(tmem + TM_N2, tmem + TM_N2A + 8 * s, D.DPK + 2 * s, D.id_k64, 1);
     mma_commit(&X.bar[B_R3]);
-    if (!wait_bar(X, B_S4, step)) return false;
+    if (!warp_wait(X, B_S4, step)) return false;
     tc_fence_after();
 #pragma unroll
     for (int s = 0; s < 4; ++s)
         mma_ts(tmem + TM_N2, tmem + TM_NA + 8 * s, D.YB + 128 * s, D.id_mn_neg, 1);
     mma_commit(&X.bar[B_R4]);
-    if (!wait_bar(X, B_T, step)) return false;
+    if (!warp_wait(X, B_T, step)) return false;
     tc_fence_after();
     // W^T (unscaled) = Kr^T T^T: A = Kr hi as K-major [ch][tok], B = T [r][i].
 #pragma unroll
