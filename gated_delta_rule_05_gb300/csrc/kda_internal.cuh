@@ -60,9 +60,13 @@ inline bool split_plan(int32_t num_seqs, int32_t H, int sms, SplitPlan* plan) {
     p.units = (int32_t)units;
     p.producers = sms - p.units;
     // Producers claim chunks in chunk-major order, so about producers / units
-    // chunks of each unit are in flight; the ring holds twice that.
+    // chunks of each unit are being computed; each producer may also hold its
+    // next claim and a finished job not yet published.  The ring holds three
+    // times producers / units plus the consumer's own pipeline: with fewer
+    // slots, producers block on full slots while holding jobs other consumers
+    // wait for, and the launch slows down by about half.
     const int ahead = (p.producers + p.units - 1) / p.units;
-    p.ring = 2 * ahead + 2;
+    p.ring = 3 * ahead + 4;
     if (p.ring < 4) p.ring = 4;
     if (p.ring > kSplitMaxRing) p.ring = kSplitMaxRing;
     p.flags_off = workspace_bytes(num_seqs);

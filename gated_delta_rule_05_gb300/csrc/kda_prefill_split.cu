@@ -80,11 +80,12 @@ static_assert(OFF_JOB + 2 * sizeof(JobDesc) <= OFF_GL, "job area overflows");
 // Producer-only uses of space that only the single-CTA kernel's back phases
 // need.  The g tile lives apart from the Gram lo parts and solve tiles (which
 // reuse OFF_G), so that the next job's q / k / g load can start as soon as
-// pass B is done.  (e^G Q)^T, Ktil^T, P and T are staged in shared memory and
-// sent to the ring with bulk copies: written straight from registers, each
-// warp store of the swizzled tiles would touch 32 different lines.
+// pass B is done.  The operand tiles are staged in shared memory and sent to
+// the ring with bulk copies (e^{G_last} from OFF_GL): written straight from
+// registers, each warp store of the swizzled tiles would touch 32 different
+// lines.
 constexpr uint32_t P_G = OFF_WT;          // g tile [64][128] fp32
-constexpr uint32_t P_QG = OFF_V;          // (e^G Q)^T staging, 16 KB
+constexpr uint32_t P_QG = OFF_V;          // (e^G Q)^T staging, then -W^T staging, 16 KB
 constexpr uint32_t P_KT = OFF_KT;         // Ktil^T staging, 16 KB
 constexpr uint32_t P_P = OFF_P;           // P staging, 8 KB
 constexpr uint32_t P_T16 = OFF_T16;       // T staging, 8 KB (the decay stats' space)
@@ -411,14 +412,24 @@ __device__ __forceinline__ void producer(const Ctx& X, uint32_t tmem, int warp, 
         const int ct = t.ct;
         const int32_t* consumed = flags + (size_t)U * R;
         int step = 0;
+        // Job jc - 1 is handed to the data-movement warp (JOB_DONE) during
+        // job jc, once pass B is done: by then ct 0's last bulk copies have
+        // completed, and the group is waiting for the Gram product anyway.
+        // It is always handed over before job jc writes its own ring slot
+        // (a later chunk of the same unit may need job jc - 1).
+        auto job_done = [&](int jc_done, int npass_done) {
+            bulk_wait_group0();
+            fence_proxy_async_global();
+            jd[jc_done & 1].npass = npass_done;
+            mbar_arrive(&X.bar[B_JOB_DONE]);
+        };
+        int prev_npass = 0;
         for (int jc = 0;; ++jc) {
-            // The previous job's T copy has read its staging area (the decay
-            // stats go there) before the group passes the barrier below.
-            if (ct == 0) bulk_wait_group_read0();
             if (!group_wait(X, B_QKG_FULL, jc)) break;
             const JobDesc job = jd[jc & 1];
             if (job.terminate) {
                 if (ct == 0) {
+                    if (jc > 0) job_done(jc - 1, prev_npass);
                     X.desc[step & 1].last_step = 1;
                     mbar_arrive(&X.bar[B_OPS]);        // lets the MMA warp finish
                 }
@@ -428,36 +439,47 @@ __device__ __forceinline__ void producer(const Ctx& X, uint32_t tmem, int warp, 
             const int len = (job.eos - t0 < kC) ? (int)(job.eos - t0) : kC;
             uint8_t* slot = ring + ((size_t)job.u * R + job.c % R) * 2 * kStage;
             // The slot is free once the consumer has copied out chunk c - R.
-            if (ct == 0 && job.c >= R) {
-                int32_t seen;
-                const int32_t want = job.c - R + 1;
-                if (!poll_flag(X, consumed + job.u, [&](int32_t v) { return v >= want; }, &seen))
-                    atomicExch(&X.misc->abort, 1);
-            }
+            // A first look is issued now and checked after pass B.
+            const int32_t want = job.c - R + 1;
+            int32_t seen = (ct == 0 && job.c >= R) ? ld_relaxed_gpu(consumed + job.u) : want;
             float2 Gq[16];
             PassParams pp;
             const int npass = gate_prep(X, t, len, reinterpret_cast<const float*>(sm + P_G), Gq, pp);
-            if (*reinterpret_cast<volatile int32_t*>(&X.misc->abort)) break;
             bool alive = true;
             for (int p = 0; p < npass; ++p) {
                 const Pass ps = select_pass(pp, p, npass, len);
                 uint8_t* blk = slot + (size_t)p * kStage;
-                pass_factors(X, t, ps, reinterpret_cast<float*>(blk + BLK_GL));
                 if (ct == 0) {
                     X.desc[step & 1].last_step = 0;
                     bulk_wait_group_read0();       // staging areas free again
                 }
                 group_sync();
+                pass_factors(X, t, ps, reinterpret_cast<float*>(sm + OFF_GL));
                 gram_operands(X, t, ps, Gq, sm + P_QG, sm + P_KT);
                 fence_proxy_async_smem();
                 group_sync();
                 if (ct == 0) {
                     mbar_arrive(&X.bar[B_OPS]);
-                    // q, k, g and beta are read: the next job may load.
+                    bool free_slot = true;
+                    if (p == 0) {
+                        if (jc > 0) job_done(jc - 1, prev_npass);
+                        if (seen < want)
+                            free_slot = poll_flag(X, consumed + job.u,
+                                                  [&](int32_t v) { return v >= want; }, &seen);
+                        fence_acq_rel_gpu();
+                    }
+                    // q, k, g and beta are read: the next job may be claimed
+                    // and loaded.  (Only now: a producer that waits for a
+                    // slot holds no further claim that a consumer may need.)
                     if (p == npass - 1) mbar_arrive(&X.bar[B_QKG_EMPTY]);
-                    bulk_store(blk + BLK_QG, sm + P_QG, 16384);
-                    bulk_store(blk + BLK_KT, sm + P_KT, 16384);
-                    bulk_commit_group();
+                    if (free_slot) {
+                        bulk_store(blk + BLK_QG, sm + P_QG, 16384);
+                        bulk_store(blk + BLK_KT, sm + P_KT, 16384);
+                        bulk_store(blk + BLK_GL, sm + OFF_GL, 512);
+                        bulk_commit_group();
+                    } else {
+                        atomicExch(&X.misc->abort, 1);   // the group stops at its next wait
+                    }
                 }
                 if (!gram_readout(X, t, tmem, ps.lo, ps.hi, step, sm + P_P)) { alive = false; break; }
                 if (ct == 0) {
@@ -468,21 +490,19 @@ __device__ __forceinline__ void producer(const Ctx& X, uint32_t tmem, int warp, 
                 if (ct == 0) {
                     bulk_store(blk + BLK_T16, sm + P_T16, 8192);
                     bulk_commit_group();
+                    // -W^T reuses the (e^G Q)^T staging area: its copy (the
+                    // oldest of the three groups in flight) has read it.
+                    bulk_wait_group_read2();
                 }
-                if (!w_readout(X, t, tmem, step, blk + BLK_WT)) { alive = false; break; }
+                if (!w_readout(X, t, tmem, step, sm + P_QG)) { alive = false; break; }
+                if (ct == 0) {
+                    bulk_store(blk + BLK_WT, sm + P_QG, 16384);
+                    bulk_commit_group();
+                }
                 ++step;
             }
             if (!alive) break;
-            // Every thread's direct stores (-W^T, e^{G_last}) precede this
-            // point (the group barrier at the end of w_readout), and ct 0's
-            // bulk copies have completed; the data-movement warp publishes
-            // the slot.
-            if (ct == 0) {
-                bulk_wait_group0();
-                fence_proxy_async_global();
-                jd[jc & 1].npass = npass;
-                mbar_arrive(&X.bar[B_JOB_DONE]);
-            }
+            prev_npass = npass;
         }
     }
 }

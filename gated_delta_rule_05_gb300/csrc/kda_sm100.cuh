@@ -151,6 +151,13 @@ __device__ __forceinline__ void bulk_wait_group_read0()
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
+// Waits until at most two of this thread's committed bulk groups have not
+// yet read their source.
+__device__ __forceinline__ void bulk_wait_group_read2()
+{
+    asm volatile("cp.async.bulk.wait_group.read 2;" ::: "memory");
+}
+
 // Waits until every committed bulk store of this thread has completed.
 __device__ __forceinline__ void bulk_wait_group0()
 {

@@ -38,12 +38,14 @@
 // entries are assumed to stay inside the fp16 range (|x| < 65504).
 //
 // UT solve.  With D the inverse of the 16 x 16 diagonal blocks of L = I + A
-// (forward substitution on CUDA cores) and N = D A_off (A_off = the blocks
-// below the diagonal), N is nilpotent of order 4, so
-//     (I + A)^{-1} = (I + N)^{-1} D = (I - N)(I + N^2) D,
-// and T = (I - N)(I + N^2) D' with D' = D Diag(b).  The products N = D A_off,
-// N^2, Y = D' + N^2 D' and T = Y - N Y run on the tensor cores (fp16 operands)
-// in tensor memory and shared memory idle at that point of the chunk.
+// and N = D A_off (A_off = the blocks below the diagonal), N is nilpotent of
+// order 4, so
+//     (I + A)^{-1} = (I + N)^{-1} D = (I + N^2)(I - N) D,
+// and T = (I + N^2) Z with Z = (I - N) D', D' = D Diag(b).  D (forward
+// substitution) and N (six 16 x 16 block products) are formed on CUDA cores;
+// N^2 and Z are one round of tensor-core products, T = (I + N^2) Z a second
+// (fp16 operands, in tensor memory and shared memory idle at that point of
+// the chunk).
 #pragma once
 
 #include <cuda.h>
@@ -82,13 +84,13 @@ constexpr uint32_t OFF_BDLO = OFF_A32; //   Gram readout: Gram B lo part [ch][Kc
 constexpr uint32_t OFF_T16 = 214016;   // T       [r][i] fp16 (V product); during gate prep:
 constexpr uint32_t OFF_STAT = OFF_T16; //   per row-quarter decay stats, fp32 [3][4][128]
 constexpr uint32_t OFF_Y = 222208;     // 3 KB not used by the phases
-// Solve tiles, all fp16, in regions idle during the solve (the g tile's and
-// the Gram B tile's space; the next q/k/g load waits for them):
-constexpr uint32_t OFF_DM = OFF_G;            // D  as MN-major A [k][r]
-constexpr uint32_t OFF_AO = OFF_G + 8192;     // A_off as MN-major B [k][c]
-constexpr uint32_t OFF_NB = OFF_G + 16384;    // N  as MN-major B [m][c]
-constexpr uint32_t OFF_DPK = OFF_G + 24576;   // D' as K-major B [c][m] (column c of D')
-constexpr uint32_t OFF_YB = OFF_BD;           // Y  as MN-major B [m][c]
+// Solve tiles, in regions idle during the solve (the g tile's and the Gram
+// B tile's space; the next q/k/g load waits for the first three):
+constexpr uint32_t OFF_DF = OFF_G;            // D blocks, fp32 [4][16][17] (padded rows)
+constexpr uint32_t OFF_IMN = OFF_G + 8192;    // I - N as K-major fp16 A [r][k]
+constexpr uint32_t OFF_NB = OFF_G + 16384;    // N  as MN-major fp16 B [m][c] = K-major A [r][k]
+constexpr uint32_t OFF_DPK = OFF_G + 24576;   // D' as K-major fp16 B [c][m] (column c of D')
+constexpr uint32_t OFF_ZB = OFF_BD;           // Z  as MN-major fp16 B [m][c]
 constexpr uint32_t OFF_OST = OFF_A32;  // O tile staging of the single-CTA kernel
 constexpr uint32_t OFF_GL = 225280;    // e^{G_last} per channel
 constexpr uint32_t OFF_R = 225792;     // 2^R per channel
@@ -115,7 +117,7 @@ constexpr uint32_t kBlkBytes = 66048;
 enum Bar {
     B_QKG_FULL = 0, B_QKG_EMPTY, B_V_FULL, B_V_EMPTY, B_OPS, B_MMA_G, B_T, B_MMA_W,
     B_CV, B_MMA_C, B_U, B_MMA_OS,
-    B_S1, B_R1, B_S2, B_R2, B_S3, B_R3, B_S4, B_R4,   // UT solve rounds
+    B_S1, B_R1, B_S2, B_R2,                            // UT solve rounds
     B_JOB_DONE,                                        // split producer: operands written
     B_SV_FULL0, B_SV_FULL1, B_SV_FULL2, B_SV_FULL3,    // split consumer: v tile buffers
     B_SV_EMPTY0, B_SV_EMPTY1, B_SV_EMPTY2, B_SV_EMPTY3,
@@ -135,11 +137,10 @@ constexpr uint32_t TM_S = 320;    // S^T fp32 [v][ch]                           
 constexpr uint32_t TM_UB = 448;   // U^T fp16 A operand                           32 cols
 constexpr uint32_t kTmemCols = 512;
 // During the UT solve (rows 0..63 used), in columns otherwise idle then:
-constexpr uint32_t TM_N = 0;      // N = D A_off, fp32
-constexpr uint32_t TM_N2A = 64;   // N^2 as fp16 A operand
-constexpr uint32_t TM_IA = 96;    // identity rows as fp16 A operand
-constexpr uint32_t TM_NA = TM_UB; // N as fp16 A operand
-constexpr uint32_t TM_N2 = TM_C;  // N^2, fp32; then Y, then T
+constexpr uint32_t TM_Z = 0;      // Z = (I - N) D', fp32                         64 cols
+constexpr uint32_t TM_N2 = 64;    // N^2, fp32                                    64 cols
+constexpr uint32_t TM_T = TM_C;   // T = (I + N^2) Z, fp32                        64 cols
+constexpr uint32_t TM_IPN = TM_UB;  // I + N^2 as fp16 A operand                  32 cols
 
 struct StepDesc {
     int32_t t0, len, lo, hi, first_pass, last_pass, last_step, chunk;
@@ -518,31 +519,37 @@ __device__ __forceinline__ bool gram_readout(const Ctx& X, const Lane& t, uint32
     return true;
 }
 
-// Front phase 5: the UT solve (CUDA-core part of each round; the MMA warp
-// runs the products, mma_front below).  Leaves T as bf16 in shared memory
-// (the W product) and as fp16 at t16_dst.  Arrives B_QKG_EMPTY after the
-// third round when `release_qkg` (the q / k / g tiles are no longer read) and
-// B_T at the end.
+// Front phase 5: the UT solve (CUDA-core part; the MMA warp runs the two
+// product rounds, mma_front below).  Leaves T as bf16 in shared memory (the
+// W product) and as fp16 at t16_dst.  Arrives B_QKG_EMPTY after the first
+// round when `release_qkg` (the g tile's space is no longer read) and B_T at
+// the end.
 __device__ __forceinline__ bool ut_solve(const Ctx& X, const Lane& t, uint32_t tmem, int warp,
                                          int step, bool release_qkg, uint8_t* t16_dst)
 {
     uint8_t* sm = X.sm;
     const float* sBst = reinterpret_cast<const float*>(sm + OFF_BST);
     const float* sA = reinterpret_cast<const float*>(sm + OFF_A32);
+    float* sD = reinterpret_cast<float*>(sm + OFF_DF);
     const int ct = t.ct, L = t.L, half = t.half;
     const uint32_t lane_base = t.lane_base;
-    // S1: diagonal-block inverses D (warps of ct < 128), A_off as fp16 and
-    // identity rows in TMEM (the other warps).
+    const bool top = (warp & 3) < 2;         // this warp holds rows 0..63
+    // S1a: diagonal-block inverses (warps of ct < 128, one column each): D
+    // in fp32 and D' = D Diag(b) as the K-major fp16 B tile.  Meanwhile the
+    // other warps fill the chunks of the N and I - N tiles that lie in
+    // diagonal or upper blocks (zero in N; identity or zero in I - N).
     if (ct < 128) {
         const int b = ct >> 5, j = ct & 31;
         float x[16];
         diag_block_column(sA, b, j, x);
         if (j < 16) {
-            const int k = 16 * b + j;        // column k of D = row k of the tiles
+            const int k = 16 * b + j;        // column k of D = row k of the D' tile
             const float bk = sBst[k];
 #pragma unroll
+            for (int r = 0; r < 16; ++r) sD[(16 * b + r) * 17 + j] = x[r];
+#pragma unroll
             for (int c8 = 0; c8 < 8; ++c8) {
-                uint32_t pd[4], pq[4];
+                uint32_t pq[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     float dv[2];
@@ -551,93 +558,108 @@ __device__ __forceinline__ bool ut_solve(const Ctx& X, const Lane& t, uint32_t t
                         const int r = 8 * c8 + 2 * e + u;
                         dv[u] = ((r >> 4) == b) ? x[r & 15] : 0.f;
                     }
-                    pd[e] = pack_f16x2(dv[0], dv[1]);
                     pq[e] = pack_f16x2(dv[0] * bk, dv[1] * bk);
                 }
-                st_chunk(sm + OFF_DM, k, c8, make_uint4(pd[0], pd[1], pd[2], pd[3]));
                 st_chunk(sm + OFF_DPK, k, c8, make_uint4(pq[0], pq[1], pq[2], pq[3]));
             }
         }
     } else {
-        const int k = (ct - 128) >> 1, hh = ct & 1;
+        // row R, column blocks 2 jb .. 2 jb + 1 of 16 (chunks 4 jb .. 4 jb + 3)
+        const int R = (ct - 128) >> 1, jb = (ct - 128) & 1;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            uint32_t pk[4];
+        for (int cb = 0; cb < 2; ++cb) {
+            const int blk16 = 2 * jb + cb;
+            if (blk16 >= (R >> 4)) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int c0 = 32 * hh + 8 * j + 2 * e;
-                const float a0 = ((c0 >> 4) < (k >> 4)) ? sA[k * LDA + c0] : 0.f;
-                const float a1 = (((c0 + 1) >> 4) < (k >> 4)) ? sA[k * LDA + c0 + 1] : 0.f;
-                pk[e] = pack_f16x2(a0, a1);
+                for (int h8 = 0; h8 < 2; ++h8) {
+                    const int chunk = 2 * blk16 + h8;
+                    st_chunk(sm + OFF_NB, R, chunk, make_uint4(0, 0, 0, 0));
+                    // the 1 of I - N: column R, in chunk R / 8 at position R % 8
+                    uint32_t w[4] = {0, 0, 0, 0};
+                    if (chunk == (R >> 3)) w[(R & 7) >> 1] = (R & 1) ? 0x3C000000u : 0x3C00u;
+                    st_chunk(sm + OFF_IMN, R, chunk, make_uint4(w[0], w[1], w[2], w[3]));
+                }
             }
-            st_chunk(sm + OFF_AO, k, 4 * hh + j, make_uint4(pk[0], pk[1], pk[2], pk[3]));
         }
-        if ((warp & 3) < 2) {                // lanes 0..63: identity rows
-            uint32_t id[32];
+    }
+    group_sync();
+    // S1b: N = D A_off, whose non-zero blocks are N_ij = D_ii A_ij for
+    // (i, j) = (1,0) (2,0) (2,1) (3,0) (3,1) (3,2): 6 x 16 rows x 8 column
+    // pairs = 768 segments, three per thread (computed together), written
+    // (fp16) to the N tile and, negated, to the I - N tile.  Both tiles serve
+    // as K-major A operands of the first product round (the N tile also as
+    // its MN-major B operand).
+    {
+        const float* drow[3];
+        const float* acol[3];
+        uint32_t off[3];
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-                id[i] = ((2 * i == L) ? 0x3C00u : 0u) | ((2 * i + 1 == L) ? 0x3C000000u : 0u);
-            tmem_st32(tmem + lane_base + TM_IA, id);
-            tmem_st_wait();
+        for (int rep = 0; rep < 3; ++rep) {
+            const int sgi = ct + 256 * rep;
+            const int b6 = sgi >> 7, rr = (sgi >> 3) & 15, cpair = sgi & 7;
+            const int bi = (b6 == 0) ? 1 : ((b6 < 3) ? 2 : 3);
+            const int bj = (b6 == 0) ? 0 : ((b6 < 3) ? b6 - 1 : b6 - 3);
+            drow[rep] = sD + (16 * bi + rr) * 17;
+            acol[rep] = sA + (16 * bi) * LDA + 16 * bj + 2 * cpair;
+            const int R = 16 * bi + rr, col = 16 * bj + 2 * cpair, chunk = col >> 3;
+            off[rep] = (R >> 3) * 1024 + (R & 7) * 128 + ((chunk ^ (R & 7)) << 4) + (col & 7) * 2;
+        }
+        float n[3][2];
+#pragma unroll
+        for (int rep = 0; rep < 3; ++rep) n[rep][0] = n[rep][1] = 0.f;
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+#pragma unroll
+            for (int rep = 0; rep < 3; ++rep) {
+                const float d = drow[rep][m];
+                const float2 a = *reinterpret_cast<const float2*>(acol[rep] + m * LDA);
+                n[rep][0] = fmaf(d, a.x, n[rep][0]);
+                n[rep][1] = fmaf(d, a.y, n[rep][1]);
+            }
+        }
+#pragma unroll
+        for (int rep = 0; rep < 3; ++rep) {
+            *reinterpret_cast<uint32_t*>(sm + OFF_NB + off[rep]) = pack_f16x2(n[rep][0], n[rep][1]);
+            *reinterpret_cast<uint32_t*>(sm + OFF_IMN + off[rep]) = pack_f16x2(-n[rep][0], -n[rep][1]);
         }
     }
     fence_proxy_async_smem();
-    tc_fence_before();
     group_sync();
     if (ct == 0) mbar_arrive(&X.bar[B_S1]);
-    const bool top = (warp & 3) < 2;         // this warp holds rows 0..63
-    // S2: N -> fp16 A operand (TMEM) and MN-major B tile
+    // S2: Z -> fp16 MN-major B tile; I + N^2 -> fp16 A operand.
     if (!group_wait(X, B_R1, step)) return false;
+    // The g tile's space (D, N, D' tiles) is no longer read: the next chunk may load.
+    if (ct == 0 && release_qkg) mbar_arrive(&X.bar[B_QKG_EMPTY]);
     tc_fence_after();
     if (top) {
-        uint32_t nb[16];
-        tmem_row_f16(tmem + lane_base + TM_N + 32 * half, nb);
-        tmem_st16(tmem + lane_base + TM_NA + 16 * half, nb);
+        uint32_t zb[16], d[32], ip[16];
+        tmem_row_f16(tmem + lane_base + TM_Z + 32 * half, zb);
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-            st_chunk(sm + OFF_NB, L, 4 * half + j,
-                     make_uint4(nb[4 * j], nb[4 * j + 1], nb[4 * j + 2], nb[4 * j + 3]));
+            st_chunk(sm + OFF_ZB, L, 4 * half + j,
+                     make_uint4(zb[4 * j], zb[4 * j + 1], zb[4 * j + 2], zb[4 * j + 3]));
+        tmem_ld32(tmem + lane_base + TM_N2 + 32 * half, d);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int k = 32 * half + 2 * i;
+            const float a0 = __uint_as_float(d[2 * i]) + ((k == L) ? 1.f : 0.f);
+            const float a1 = __uint_as_float(d[2 * i + 1]) + ((k + 1 == L) ? 1.f : 0.f);
+            ip[i] = pack_f16x2(a0, a1);
+        }
+        tmem_st16(tmem + lane_base + TM_IPN + 16 * half, ip);
         tmem_st_wait();
     }
     fence_proxy_async_smem();
     tc_fence_before();
     group_sync();
     if (ct == 0) mbar_arrive(&X.bar[B_S2]);
-    // S3: N^2 -> fp16 A operand
+    // S3: T -> bf16 (W product) and fp16 (V product) rows
     if (!group_wait(X, B_R2, step)) return false;
     tc_fence_after();
     if (top) {
-        uint32_t nb[16];
-        tmem_row_f16(tmem + lane_base + TM_N2 + 32 * half, nb);
-        tmem_st16(tmem + lane_base + TM_N2A + 16 * half, nb);
-        tmem_st_wait();
-    }
-    tc_fence_before();
-    group_sync();
-    if (ct == 0) mbar_arrive(&X.bar[B_S3]);
-    // S4: Y -> fp16 MN-major B tile (Y stays in TMEM as the accumulator)
-    if (!group_wait(X, B_R3, step)) return false;
-    // The g tile's space is no longer read: the next chunk may load.
-    if (ct == 0 && release_qkg) mbar_arrive(&X.bar[B_QKG_EMPTY]);
-    tc_fence_after();
-    if (top) {
-        uint32_t yb[16];
-        tmem_row_f16(tmem + lane_base + TM_N2 + 32 * half, yb);
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            st_chunk(sm + OFF_YB, L, 4 * half + j,
-                     make_uint4(yb[4 * j], yb[4 * j + 1], yb[4 * j + 2], yb[4 * j + 3]));
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    group_sync();
-    if (ct == 0) mbar_arrive(&X.bar[B_S4]);
-    // S5: T -> bf16 (W product) and fp16 (V product) rows
-    if (!group_wait(X, B_R4, step)) return false;
-    tc_fence_after();
-    if (top) {
         uint32_t d[32];
-        tmem_ld32(tmem + lane_base + TM_N2 + 32 * half, d);
+        tmem_ld32(tmem + lane_base + TM_T + 32 * half, d);
         tmem_ld_wait();
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -822,8 +844,8 @@ __device__ __forceinline__ void state_store(const Lane& t, uint32_t tmem, float*
 // MMA warp (one thread).
 
 struct FrontDescs {
-    uint64_t AD, ADLO, BDHL, ADK, T, DM, AO, NB, DPK, YB;
-    uint32_t id_g, id_w, id_r1, id_mn, id_k64, id_mn_neg;
+    uint64_t AD, ADLO, BDHL, ADK, T, NA, IMN, NB, DPK, ZB;
+    uint32_t id_g, id_w, id_mn, id_k64;
 };
 
 // Base descriptors; a K step advances the start address field (16-byte
@@ -833,26 +855,22 @@ __device__ __forceinline__ FrontDescs make_front_descs(uint8_t* sm)
     FrontDescs D;
     D.id_g = make_idesc_bf16(128, 128, true, true);     // Gram
     D.id_w = make_idesc_bf16(128, 64, false, false);    // W
-    D.id_r1 = make_idesc_f16(128, 64, true, true);
-    D.id_mn = make_idesc_f16(128, 64, false, true);     // TMEM A x MN-major B
-    D.id_k64 = make_idesc_f16(128, 64, false, false);   // TMEM A x K-major B
-    D.id_mn_neg = make_idesc_f16(128, 64, false, true, true);
+    D.id_mn = make_idesc_f16(128, 64, false, true);     // K-major A x MN-major B
+    D.id_k64 = make_idesc_f16(128, 64, false, false);   // K-major A x K-major B
     D.AD = make_sdesc(smem_u32(sm + OFF_AD), 16384, 1024, kSwizzle128B);
     D.ADLO = make_sdesc(smem_u32(sm + OFF_ADLO), 16384, 1024, kSwizzle128B);
     D.BDHL = make_sdesc(smem_u32(sm + OFF_BD), OFF_BDLO - OFF_BD, 1024, kSwizzle128B);
     D.ADK = make_sdesc(smem_u32(sm + OFF_AD), 16, 1024, kSwizzle128B);
     D.T = make_sdesc(smem_u32(sm + OFF_T), 16, 1024, kSwizzle128B);
-    // D as the A operand of N = D A_off: M = 128 with the second 64-row
-    // block pointed at the next tile (finite data; its rows are unused).
-    D.DM = make_sdesc(smem_u32(sm + OFF_DM), 8192, 1024, kSwizzle128B);
-    D.AO = make_sdesc(smem_u32(sm + OFF_AO), 8192, 1024, kSwizzle128B);
+    D.NA = make_sdesc(smem_u32(sm + OFF_NB), 16, 1024, kSwizzle128B);   // N as K-major A
+    D.IMN = make_sdesc(smem_u32(sm + OFF_IMN), 16, 1024, kSwizzle128B);
     D.NB = make_sdesc(smem_u32(sm + OFF_NB), 8192, 1024, kSwizzle128B);
     D.DPK = make_sdesc(smem_u32(sm + OFF_DPK), 16, 1024, kSwizzle128B);
-    D.YB = make_sdesc(smem_u32(sm + OFF_YB), 8192, 1024, kSwizzle128B);
+    D.ZB = make_sdesc(smem_u32(sm + OFF_ZB), 8192, 1024, kSwizzle128B);
     return D;
 }
 
-// The front products of one step, after B_OPS: the Gram, the four solve
+// The front products of one step, after B_OPS: the Gram, the two solve
 // rounds and W^T.  Called by the whole MMA warp.  Returns false if a wait
 // gave up.
 __device__ __forceinline__ bool mma_front(const Ctx& X, uint32_t tmem, const FrontDescs& D,
@@ -865,32 +883,22 @@ __device__ __forceinline__ bool mma_front(const Ctx& X, uint32_t tmem, const Fro
 #pragma unroll
     for (int s = 0; s < 8; ++s) mma_ss(tmem + TM_G, D.ADLO + 128 * s, D.BDHL + 128 * s, D.id_g, 1);
     mma_commit(&X.bar[B_MMA_G]);
-    // UT solve: N = D A_off ; N^2 = N N ; Y = I D' + N^2 D' ; T = Y - N Y.
+    // UT solve, round 1: N^2 = N N and Z = (I - N) D'; round 2: T = (I + N^2) Z.
     if (!warp_wait(X, B_S1, step)) return false;
     tc_fence_after();
+    // (M = 128 with A rows 64..127 read from the next tile: finite data,
+    // rows unused.)
 #pragma unroll
-    for (int s = 0; s < 4; ++s) mma_ss(tmem + TM_N, D.DM + 128 * s, D.AO + 128 * s, D.id_r1, s > 0);
+    for (int s = 0; s < 4; ++s) mma_ss(tmem + TM_N2, D.NA + 2 * s, D.NB + 128 * s, D.id_mn, s > 0);
+#pragma unroll
+    for (int s = 0; s < 4; ++s) mma_ss(tmem + TM_Z, D.IMN + 2 * s, D.DPK + 2 * s, D.id_k64, s > 0);
     mma_commit(&X.bar[B_R1]);
     if (!warp_wait(X, B_S2, step)) return false;
     tc_fence_after();
 #pragma unroll
     for (int s = 0; s < 4; ++s)
-        mma_ts(tmem + TM_N2, tmem + TM_NA + 8 * s, D.NB + 128 * s, D.id_mn, s > 0);
+        mma_ts(tmem + TM_T, tmem + TM_IPN + 8 * s, D.ZB + 128 * s, D.id_mn, s > 0);
     mma_commit(&X.bar[B_R2]);
-    if (!warp_wait(X, B_S3, step)) return false;
-    tc_fence_after();
-#pragma unroll
-    for (int s = 0; s < 4; ++s)
-        mma_ts(tmem + TM_N2, tmem + TM_IA + 8 * s, D.DPK + 2 * s, D.id_k64, s > 0);
-#pragma unroll
-    for (int s = 0; s < 4; ++s) mma_ts(tmem + TM_N2, tmem + TM_N2A + 8 * s, D.DPK + 2 * s, D.id_k64, 1);
-    mma_commit(&X.bar[B_R3]);
-    if (!warp_wait(X, B_S4, step)) return false;
-    tc_fence_after();
-#pragma unroll
-    for (int s = 0; s < 4; ++s)
-        mma_ts(tmem + TM_N2, tmem + TM_NA + 8 * s, D.YB + 128 * s, D.id_mn_neg, 1);
-    mma_commit(&X.bar[B_R4]);
     if (!warp_wait(X, B_T, step)) return false;
     tc_fence_after();
     // W^T (unscaled) = Kr^T T^T: A = Kr hi as K-major [ch][tok], B = T [r][i].
