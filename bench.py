@@ -42,6 +42,7 @@ if ROOT not in sys.path:
 METRIC = "KDA prefill tokens/s and decode state GB/s at H=32,d=128; % of GB300 roofline"
 PREFILL_WORKLOAD = 4          # prefill_h32_t1m
 DECODE_WORKLOAD = 5           # decode_1024x32
+VARLEN_WORKLOAD = 3           # varlen16_h32
 
 # Algorithmic work per token x head at d = 128 (counts used for the roofline):
 # bytes = q, k, v (bf16) 768 + log_alpha 512 + beta 4 + o (bf16) 256.
@@ -322,20 +323,23 @@ def run_kda(args):
         line.update(bench_prefill(args, kda, torch, synth, peaks, stream, dev, rank, world, smi_id))
     if args.only in ("all", "decode"):
         line["decode"] = bench_decode(args, kda, torch, synth, peaks, stream, dev, rank, world, smi_id)
+    if args.only in ("all", "varlen"):
+        line["varlen"] = bench_varlen(args, kda, torch, synth, peaks, stream, dev, rank, world, smi_id)
     if rank == 0:
-        if "value" not in line:        # decode only: its metric leads the line
-            d = line["decode"]
-            line.update({"metric": METRIC, "value": d["value"], "unit": "GB/s", "n_gpus": world,
+        if "value" not in line:        # decode or varlen only: that section leads the line
+            d = line["decode"] if "decode" in line else line["varlen"]
+            line.update({"metric": METRIC, "value": d["value"], "unit": d["unit"], "n_gpus": world,
                          "steps": args.steps, "warmup": args.warmup,
                          "ms_per_step": d["ms_per_step"], "higher_is_better": True,
                          "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-                         "data": "synthetic", "config": {"workload": "decode_1024x32"},
+                         "data": "synthetic", "config": {"workload": d["workload"]},
                          "roofline": d["roofline"], "clocks": d["clocks"],
                          "gpu_launches": d["gpu_launches"], "cpu_baseline": None,
                          "e2e": None})
         else:
             line["gpu_launches"] = line.get("gpu_launches", 0) + \
-                line.get("decode", {}).get("gpu_launches", 0)
+                line.get("decode", {}).get("gpu_launches", 0) + \
+                line.get("varlen", {}).get("gpu_launches", 0)
         if args.only == "all" and world == 1 and not args.no_cpu:
             line["cpu_baseline"] = cpu_baseline()   # rank 0 at N=1 only
         print(json.dumps(line), flush=True)
@@ -461,6 +465,63 @@ def bench_decode(args, kda, torch, synth, peaks, stream, dev, rank, world, smi_i
     }
 
 
+def bench_varlen(args, kda, torch, synth, peaks, stream, dev, rank, world, smi_id):
+    """varlen16_h32: 16 packed sequences x 32 heads with an initial state and
+    S_final returned.  512 (sequence, head) units: the single-CTA tensor-core
+    kernel, one CTA per unit, longest sequences first."""
+    wv = synth.WORKLOADS[VARLEN_WORKLOAD]
+    lengths = synth.draw_lengths(wv)
+    name = wv.name
+    if args.varlen_scale != 1.0:
+        lengths = [max(1, int(round(x * args.varlen_scale))) for x in lengths]
+        name = "%s_x%g" % (wv.name, args.varlen_scale)
+    vin = synth.generate(lengths, wv.H, wv.d, wv.d, dtype=wv.dtype, gate=wv.gate,
+                         q_scale=wv.q_scale, s0_std=wv.s0_std, seed=rank_seed(wv.seed, rank),
+                         device=dev)
+    N = len(vin.lengths)
+    T, H, d = vin.q.shape
+    ov = torch.empty_like(vin.v)
+    Sf = torch.empty_like(vin.S0)
+    ws = torch.empty(kda.kda_prefill_workspace_bytes(N, H, d, d), dtype=torch.uint8, device=dev)
+    kernel = prefill_kernel_name(ws.numel(), N)
+
+    def run():
+        kda.kda_prefill(vin.q, vin.k, vin.v, vin.log_alpha, vin.beta, S0=vin.S0,
+                        cu_seqlens=vin.cu_seqlens, o=ov, S_final=Sf, workspace=ws, stream=stream)
+
+    for _ in range(args.warmup):
+        run()
+    torch.cuda.synchronize(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(smi_id) as clk:
+        for s, e in ev:
+            s.record(stream)
+            run()
+            e.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier(world)
+    ms = sum(s.elapsed_time(e) for s, e in ev)
+    ms_max = max_over_ranks(ms, world, dev)
+    alg_bytes = T * H * BYTES_PER_TOKEN_HEAD + 2 * N * H * d * d * 4   # + S0 read, S_final write
+    achieved = alg_bytes / (ms / args.steps / 1e3) / 1e9
+    return {
+        "value": T * world * args.steps / (ms_max / 1e3), "unit": "tokens/s",
+        "ms_per_step": ms_max / args.steps, "workload": name, "tokens_per_step": T * world,
+        "num_seqs": N, "lengths": [int(x) for x in vin.lengths],
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                     "traffic": committed_traffic(name + "/" + kernel, PREFILL_KERNELS[kernel]),
+                     "peak_source": peaks["source"], "kernel": kernel,
+                     "algorithmic_bytes_per_launch": alg_bytes},
+        # per call: the work-list kernel + the tensor-core kernel
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk.summary(),
+    }
+
+
 def host_memory_available():
     """Bytes of host memory this process may still use (MemAvailable, bounded
     by a cgroup limit when one is set)."""
@@ -559,10 +620,12 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["kda", "reference"], default="kda")
-    ap.add_argument("--only", choices=["all", "prefill", "decode"], default="all",
+    ap.add_argument("--only", choices=["all", "prefill", "decode", "varlen"], default="all",
                     help="time only one part (profiling runs)")
     ap.add_argument("--tokens", type=int, default=0,
                     help="prefill length override (profiling runs on a smaller case)")
+    ap.add_argument("--varlen-scale", type=float, default=1.0,
+                    help="scale the varlen workload's sequence lengths (profiling a smaller case)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU baseline")
     args = ap.parse_args(argv)
