@@ -143,3 +143,75 @@ def decode_step(q, k, v, log_alpha, beta, S, nthreads: int | None = None,
     if rc != 0:
         raise ValueError("kda_oracle_decode_step rejected its arguments (rc=%d)" % rc)
     return o, S_new
+
+
+def snapshot_counts(lengths, interval: int):
+    """Snapshots per sequence for a given interval: floor(len / interval)."""
+    return [int(n) // int(interval) for n in lengths]
+
+
+def prefill_snapshots(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, interval: int = 64,
+                      nthreads: int | None = None, lib=None):
+    """The recurrence over packed sequences, also returning the state of every
+    sequence after every `interval` tokens: the prefix states a serving stack
+    caches and restores ("[논문 리뷰] Kimi K3 Technical Report", section 13, the
+    KDA-aware prefix cache; "Kimi 모델 분석", section "요약본 저장 위치").
+    Snapshot j of sequence n is the state after its first (j + 1) * interval
+    tokens; they are stacked over sequences in order.
+
+    Each sequence is run as consecutive segments of `interval` tokens, each
+    starting from the state the previous one ended in (the recurrence only
+    carries S from token to token, section 3.2).
+    Returns (o, S_final, snapshots [n_snap, H, dk, dv], offsets [N+1]).
+    """
+    q, k, v, g, b = (_c64(x) for x in (q, k, v, log_alpha, beta))
+    T, H, dk = q.shape
+    dv = v.shape[2]
+    cu = np.array([0, T], dtype=np.int64) if cu_seqlens is None else \
+        np.ascontiguousarray(cu_seqlens, dtype=np.int64)
+    N = cu.shape[0] - 1
+    interval = int(interval)
+    if interval < 1:
+        raise ValueError("interval must be positive")
+    s0 = None if S0 is None else _c64(S0)
+    o = np.empty((T, H, dv), dtype=np.float64)
+    S_final = np.empty((N, H, dk, dv), dtype=np.float64)
+    counts = snapshot_counts(np.diff(cu), interval)
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
+    snaps = np.empty((int(offsets[-1]), H, dk, dv), dtype=np.float64)
+    for n in range(N):
+        S = np.zeros((1, H, dk, dv)) if s0 is None else s0[n:n + 1].copy()
+        bos, eos = int(cu[n]), int(cu[n + 1])
+        j = 0
+        for s in range(bos, eos, interval):
+            e = min(eos, s + interval)
+            o[s:e], S = prefill(q[s:e], k[s:e], v[s:e], g[s:e], b[s:e], S0=S,
+                                nthreads=nthreads, lib=lib)
+            if e - s == interval:
+                snaps[offsets[n] + j] = S[0]
+                j += 1
+        S_final[n] = S[0]
+    return o, S_final, snaps, offsets
+
+
+def decode_multi(q, k, v, log_alpha, beta, S, nthreads: int | None = None, lib=None):
+    """Several tokens per sequence, keeping the state after every token: the
+    verification step of speculative decoding must be able to return to the
+    state after any accepted prefix, since the state is overwritten in place
+    and cannot be truncated ("[논문 리뷰] Kimi K3 Technical Report", section
+    13, speculative decoding replay; "Kimi 모델 분석", section "Dspark 투기적
+    디코딩").  q, k, log_alpha: [N, Ts, H, dk]; v: [N, Ts, H, dv];
+    beta: [N, Ts, H]; S: [N, H, dk, dv].  Token t of every sequence is one
+    decode step from the state after token t - 1.
+    Returns (o [N, Ts, H, dv], states [N, Ts, H, dk, dv])."""
+    q, k, v, g, b = (_c64(x) for x in (q, k, v, log_alpha, beta))
+    N, Ts, H, dk = q.shape
+    dv = v.shape[3]
+    o = np.empty((N, Ts, H, dv), dtype=np.float64)
+    states = np.empty((N, Ts, H, dk, dv), dtype=np.float64)
+    cur = _c64(S)
+    for t in range(Ts):
+        o[:, t], cur = decode_step(q[:, t], k[:, t], v[:, t], g[:, t], b[:, t], cur,
+                                   nthreads=nthreads, lib=lib)
+        states[:, t] = cur
+    return o, states
