@@ -7,6 +7,7 @@ not built, every call raises.
 
 Functions (same names as the C ABI):
   kda_prefill(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, ...)
+  kda_prefill_snapshots(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, *, interval, ...)
   kda_decode_step(q, k, v, log_alpha, beta, S_inout, ...)
   kda_prefill_workspace_bytes(num_seqs, H, d_k, d_v)
   kda_status_string(code)
@@ -24,7 +25,7 @@ KDA_BF16, KDA_FP32, KDA_BF16_F32OUT = 0, 1, 2
 
 # Every symbol include/kda.h declares.
 EXPORTS = ("kda_prefill_workspace_bytes", "kda_prefill", "kda_decode_step",
-           "kda_status_string", "kda_prefill_noalloc")
+           "kda_status_string", "kda_prefill_noalloc", "kda_prefill_snapshots")
 
 
 class KdaError(RuntimeError):
@@ -54,6 +55,10 @@ def _declare(lib):
                                     _i32, _i32, _i32, _i32, ctypes.c_int, _vp, _vp]
     lib.kda_status_string.restype = ctypes.c_char_p
     lib.kda_status_string.argtypes = [ctypes.c_int]
+    lib.kda_prefill_snapshots.restype = ctypes.c_int
+    lib.kda_prefill_snapshots.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                          _i32, _i64, _i32, _i32, _i32, ctypes.c_int,
+                                          _vp, _vp, _i32, _vp, _vp, _vp, _sz, _vp]
     return lib
 
 
@@ -229,3 +234,75 @@ def kda_prefill_noalloc(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, *,
     if rc != KDA_OK:
         raise KdaError(rc, "kda_prefill_noalloc")
     return o, S_final
+
+
+def snapshot_offsets(cu_seqlens, interval):
+    """snap_offsets for kda_prefill_snapshots from cu_seqlens (int32 [N+1],
+    on the device): exclusive prefix sums of floor(len_n / interval).  Index
+    bookkeeping for the caller's buffers; returns (offsets, total)."""
+    torch = _torch()
+    counts = torch.div(cu_seqlens[1:] - cu_seqlens[:-1], interval, rounding_mode="floor")
+    off = torch.zeros(cu_seqlens.shape[0], dtype=torch.int32, device=cu_seqlens.device)
+    off[1:] = torch.cumsum(counts, 0)
+    return off, int(off[-1].item())
+
+
+def kda_prefill_snapshots(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, *, interval,
+                          snap_offsets=None, snapshots=None, o=None, S_final=None,
+                          want_state=True, workspace=None, stream=None, o_dtype=None):
+    """kda_prefill that also returns the state of every sequence after every
+    ``interval`` tokens (a positive multiple of 64), for a prefix cache
+    (C ABI: kda_prefill_snapshots).  ``snapshots`` is [snap_offsets[N], H,
+    d_k, d_v] fp32, snapshot j of sequence n at snap_offsets[n] + j.  When
+    they are not given, offsets are derived from cu_seqlens and the buffer is
+    allocated (which reads the total back to the host).
+    Returns (o, S_final, snapshots, snap_offsets)."""
+    torch = _torch()
+    T, H, dk = q.shape
+    dv = v.shape[2]
+    if o_dtype is None:
+        o_dtype = o.dtype if o is not None else q.dtype
+    dt = _dtype_code(q, o_dtype)
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _check_cuda(name, t, q.dtype)
+    _check_cuda("log_alpha", log_alpha, torch.float32)
+    _check_cuda("beta", beta, torch.float32)
+    _check_cuda("S0", S0, torch.float32)
+    _check_cuda("cu_seqlens", cu_seqlens, torch.int32)
+    N = 1 if cu_seqlens is None else cu_seqlens.shape[0] - 1
+    dev = q.device
+    if snap_offsets is None and cu_seqlens is not None:
+        snap_offsets, total = snapshot_offsets(cu_seqlens, interval)
+    elif cu_seqlens is None:
+        total = T // interval if interval > 0 else 0
+    else:
+        total = int(snap_offsets[-1].item())
+    _check_cuda("snap_offsets", snap_offsets, torch.int32)
+    if snapshots is None:
+        snapshots = torch.empty((max(total, 0), H, dk, dv), dtype=torch.float32, device=dev)
+    _check_cuda("snapshots", snapshots, torch.float32)
+    if o is None:
+        o = torch.empty((T, H, dv), dtype=o_dtype, device=dev)
+    _check_cuda("o", o, o_dtype)
+    if S_final is None and want_state:
+        S_final = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
+    _check_cuda("S_final", S_final, torch.float32)
+    need = kda_prefill_workspace_bytes(N, H, dk, dv)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    _check_cuda("workspace", workspace)
+    # No snapshot is due (every sequence shorter than the interval): the C ABI
+    # still wants a buffer, which is never written.
+    snap_buf = snapshots if snapshots.numel() > 0 else \
+        torch.empty(4, dtype=torch.float32, device=dev)
+    snap_ptr = _ptr(snap_buf)
+    with torch.cuda.device(dev):
+        rc = lib().kda_prefill_snapshots(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(S0),
+            _ptr(cu_seqlens), N, T, H, dk, dv, dt, _ptr(o), _ptr(S_final),
+            int(interval), _ptr(snap_offsets), snap_ptr,
+            _ptr(workspace), workspace.numel() * workspace.element_size(),
+            _stream_handle(stream, dev))
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_prefill_snapshots")
+    return o, S_final, snapshots, snap_offsets

@@ -57,13 +57,16 @@ size_t kda_prefill_workspace_bytes(int32_t num_seqs, int32_t H, int32_t d_k,
     return kda::workspace_bytes(num_seqs);
 }
 
-kda_status_t kda_prefill(const void* q, const void* k, const void* v,
-                         const float* log_alpha, const float* beta,
-                         const float* S0, const int32_t* cu_seqlens,
-                         int32_t num_seqs, int64_t total_tokens, int32_t H,
-                         int32_t d_k, int32_t d_v, kda_dtype_t dtype, void* o,
-                         float* S_final, void* workspace, size_t workspace_bytes,
-                         cudaStream_t stream)
+}  // extern "C"
+
+namespace {
+
+kda_status_t prefill_impl(const void* q, const void* k, const void* v, const float* log_alpha,
+                          const float* beta, const float* S0, const int32_t* cu_seqlens,
+                          int32_t num_seqs, int64_t total_tokens, int32_t H, int32_t d_k,
+                          int32_t d_v, kda_dtype_t dtype, void* o, float* S_final,
+                          const kda::SnapArgs& snap, void* workspace, size_t workspace_bytes,
+                          cudaStream_t stream)
 {
     if (!valid_dtype(dtype)) return KDA_ERR_UNSUPPORTED;
     if (d_k != d_v || !supported_d(d_k)) return KDA_ERR_UNSUPPORTED;
@@ -73,7 +76,7 @@ kda_status_t kda_prefill(const void* q, const void* k, const void* v,
     if (total_tokens > INT32_MAX) return KDA_ERR_INVALID_ARG;
     if (total_tokens > 0 && (!q || !k || !v || !log_alpha || !beta || !o))
         return KDA_ERR_INVALID_ARG;
-    const void* ptrs16[] = {q, k, v, log_alpha, o, S0, S_final};
+    const void* ptrs16[] = {q, k, v, log_alpha, o, S0, S_final, snap.out};
     for (const void* p : ptrs16)
         if (p && !aligned(p, 16)) return KDA_ERR_INVALID_ARG;
     if (beta && !aligned(beta, 4)) return KDA_ERR_INVALID_ARG;
@@ -101,12 +104,13 @@ kda_status_t kda_prefill(const void* q, const void* k, const void* v,
             split ? reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + plan.flags_off)
                   : nullptr;
         const int32_t nflags = split ? plan.units * (plan.ring + 1) : 0;
-        err = kda::launch_worklist(cu_seqlens, num_seqs, total_tokens, ws, flags, nflags, stream);
+        err = kda::launch_worklist(cu_seqlens, num_seqs, total_tokens, ws, flags, nflags, snap,
+                                   stream);
         if (err != cudaSuccess) return KDA_ERR_CUDA;
     }
     if (split) {
         err = kda::launch_prefill_split(q, k, v, log_alpha, beta, S0, cu_seqlens, num_seqs,
-                                        total_tokens, H, dtype, o, S_final, ws, plan, stream);
+                                        total_tokens, H, dtype, o, S_final, ws, plan, snap, stream);
         if (err == cudaSuccess) return KDA_OK;
         // The launch was refused (a configuration error, nothing ran): the
         // single-CTA kernel computes the same result.
@@ -114,11 +118,55 @@ kda_status_t kda_prefill(const void* q, const void* k, const void* v,
     }
     if (tc)
         err = kda::launch_prefill_tc(q, k, v, log_alpha, beta, S0, cu_seqlens, num_seqs,
-                                     total_tokens, H, dtype, o, S_final, ws, stream);
+                                     total_tokens, H, dtype, o, S_final, ws, snap, stream);
     else
         err = kda::launch_prefill_simt(q, k, v, log_alpha, beta, S0, cu_seqlens, num_seqs,
-                                       total_tokens, H, d_k, dtype, o, S_final, ws, stream);
+                                       total_tokens, H, d_k, dtype, o, S_final, ws, snap, stream);
     return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+kda_status_t kda_prefill(const void* q, const void* k, const void* v,
+                         const float* log_alpha, const float* beta,
+                         const float* S0, const int32_t* cu_seqlens,
+                         int32_t num_seqs, int64_t total_tokens, int32_t H,
+                         int32_t d_k, int32_t d_v, kda_dtype_t dtype, void* o,
+                         float* S_final, void* workspace, size_t workspace_bytes,
+                         cudaStream_t stream)
+{
+    const kda::SnapArgs none{0, nullptr, nullptr};
+    return prefill_impl(q, k, v, log_alpha, beta, S0, cu_seqlens, num_seqs, total_tokens, H, d_k,
+                        d_v, dtype, o, S_final, none, workspace, workspace_bytes, stream);
+}
+
+kda_status_t kda_prefill_snapshots(const void* q, const void* k, const void* v,
+                                   const float* log_alpha, const float* beta, const float* S0,
+                                   const int32_t* cu_seqlens, int32_t num_seqs,
+                                   int64_t total_tokens, int32_t H, int32_t d_k, int32_t d_v,
+                                   kda_dtype_t dtype, void* o, float* S_final, int32_t interval,
+                                   const int32_t* snap_offsets, float* snapshots, void* workspace,
+                                   size_t workspace_bytes, cudaStream_t stream)
+{
+    if (interval <= 0 || interval % 64 != 0) return KDA_ERR_INVALID_ARG;
+    if (snapshots == nullptr) return KDA_ERR_INVALID_ARG;
+    if (cu_seqlens != nullptr && (snap_offsets == nullptr || !aligned(snap_offsets, 4)))
+        return KDA_ERR_INVALID_ARG;
+    if (cu_seqlens == nullptr && total_tokens > 0) {
+        // one sequence: its floor(T / interval) snapshots must not overlap o or S_final
+        const size_t snap_bytes = (size_t)(total_tokens / interval) * H * d_k * d_v * sizeof(float);
+        const size_t state_bytes = (size_t)H * d_k * d_v * sizeof(float);
+        if (o && overlaps(snapshots, snap_bytes, o,
+                          (size_t)total_tokens * H * d_v * out_bytes(dtype)))
+            return KDA_ERR_INVALID_ARG;
+        if (S_final && overlaps(snapshots, snap_bytes, S_final, state_bytes))
+            return KDA_ERR_INVALID_ARG;
+    }
+    const kda::SnapArgs snap{interval, cu_seqlens ? snap_offsets : nullptr, snapshots};
+    return prefill_impl(q, k, v, log_alpha, beta, S0, cu_seqlens, num_seqs, total_tokens, H, d_k,
+                        d_v, dtype, o, S_final, snap, workspace, workspace_bytes, stream);
 }
 
 kda_status_t kda_decode_step(const void* q, const void* k, const void* v,

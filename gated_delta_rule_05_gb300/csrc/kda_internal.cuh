@@ -80,6 +80,17 @@ inline bool split_plan(int32_t num_seqs, int32_t H, int sms, SplitPlan* plan) {
 // Number of SMs of the current device (cached per device; 0 on failure).
 int device_sm_count();
 
+// Prefix-state snapshots requested from a prefill (interval 0: none).
+// Snapshot j of sequence n, the state after its first (j + 1) * interval
+// tokens, goes to out + ((offsets[n] + j) * H + h) * d_k * d_v; offsets is
+// null for a single sequence (offset 0).  interval is a multiple of 64, so
+// every snapshot falls on a chunk boundary of every path.
+struct SnapArgs {
+    int32_t interval;
+    const int32_t* offsets;
+    float* out;
+};
+
 // KDA_DEBUG set in the environment: failing host-side steps are reported on
 // stderr (the status codes stay the same).
 inline bool debug_enabled() { return getenv("KDA_DEBUG") != nullptr; }
@@ -91,11 +102,12 @@ __device__ __forceinline__ void st_f(float* p, float x) { *p = x; }
 __device__ __forceinline__ void st_f(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
 
 // Launchers (return cudaGetLastError() after enqueueing).
-// Validates cu_seqlens (when given), writes order[], the error word and the
+// Validates cu_seqlens (when given) and the snapshot offsets (when snapshots
+// are requested with cu_seqlens), writes order[], the error word and the
 // longest length, resets the counters and zeroes `nflags` words at `flags`.
 cudaError_t launch_worklist(const int32_t* cu_seqlens, int32_t num_seqs,
                             int64_t total_tokens, int32_t* ws, int32_t* flags,
-                            int32_t nflags, cudaStream_t stream);
+                            int32_t nflags, const SnapArgs& snap, cudaStream_t stream);
 
 cudaError_t launch_decode(const void* q, const void* k, const void* v,
                           const float* log_alpha, const float* beta, float* S,
@@ -107,7 +119,7 @@ cudaError_t launch_prefill_simt(const void* q, const void* k, const void* v,
                                 const float* S0, const int32_t* cu_seqlens,
                                 int32_t num_seqs, int64_t total_tokens, int32_t H,
                                 int32_t d, kda_dtype_t dtype, void* o,
-                                float* S_final, const int32_t* ws,
+                                float* S_final, const int32_t* ws, const SnapArgs& snap,
                                 cudaStream_t stream);
 
 // Tensor-core prefill (bf16 q/k/v, d = 128).  Returns false when the call
@@ -119,13 +131,13 @@ cudaError_t launch_prefill_tc(const void* q, const void* k, const void* v,
                               const float* log_alpha, const float* beta, const float* S0,
                               const int32_t* cu_seqlens, int32_t num_seqs, int64_t total_tokens,
                               int32_t H, kda_dtype_t dtype, void* o, float* S_final,
-                              int32_t* ws, cudaStream_t stream);
+                              int32_t* ws, const SnapArgs& snap, cudaStream_t stream);
 
 cudaError_t launch_prefill_split(const void* q, const void* k, const void* v,
                                  const float* log_alpha, const float* beta, const float* S0,
                                  const int32_t* cu_seqlens, int32_t num_seqs,
                                  int64_t total_tokens, int32_t H, kda_dtype_t dtype, void* o,
                                  float* S_final, int32_t* ws, const SplitPlan& plan,
-                                 cudaStream_t stream);
+                                 const SnapArgs& snap, cudaStream_t stream);
 
 }  // namespace kda

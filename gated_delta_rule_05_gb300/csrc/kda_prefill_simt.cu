@@ -61,7 +61,8 @@ prefill_simt_kernel(const TI* __restrict__ q, const TI* __restrict__ k,
                     const float* __restrict__ beta, const float* S0,
                     const int32_t* __restrict__ cu, const int32_t* __restrict__ ws,
                     long long total_tokens, int H, TO* __restrict__ o,
-                    float* S_final)   // may alias S0: no __restrict__ on either
+                    float* S_final,   // may alias S0: no __restrict__ on either
+                    const SnapArgs snap)
 {
     using L = SimtSmem<DK, DVS>;
     constexpr int LD = L::LD, LDS = L::LDS;
@@ -97,6 +98,7 @@ prefill_simt_kernel(const TI* __restrict__ q, const TI* __restrict__ k,
         eos = cu[n + 1];
     }
     const long long sbase = ((long long)n * H + h) * DK * DV;
+    const int seq_off = (cu != nullptr && snap.interval > 0) ? snap.offsets[n] : 0;
 
     for (int e = tid; e < DK * DVS; e += kThreads) {
         const int c = e / DVS, j = e % DVS;
@@ -187,7 +189,8 @@ prefill_simt_kernel(const TI* __restrict__ q, const TI* __restrict__ k,
         }
         __syncthreads();
 
-        // Phase 4: outputs and the state carry.
+        // Phase 4: outputs and the state carry (and a prefix snapshot when a
+        // full chunk ends on a multiple of the snapshot interval).
         for (int e = tid; e < kC * DVS; e += kThreads) {
             const int r = e / DVS, j = e % DVS;
             const long long t = t0 + r;
@@ -196,12 +199,17 @@ prefill_simt_kernel(const TI* __restrict__ q, const TI* __restrict__ k,
             for (int i = 0; i <= r; ++i) acc = fmaf(sP[r * (kC + 1) + i], sU[i * LDS + j], acc);
             st_f(o + (t * H + h) * DV + col0 + j, acc);
         }
+        float* snp = nullptr;
+        if (snap.interval > 0 && t0 + kC <= eos && (t0 + kC - bos) % snap.interval == 0)
+            snp = snap.out + ((long long)(seq_off + (t0 + kC - bos) / snap.interval - 1) * H + h) *
+                                 DK * DV;
         for (int e = tid; e < DK * DVS; e += kThreads) {
             const int c = e / DVS, j = e % DVS;
             float s = sGl[c] * sS[c * LDS + j];
 #pragma unroll
             for (int r = 0; r < kC; ++r) s = fmaf(sKt[r * LD + c], sU[r * LDS + j], s);
             sS[c * LDS + j] = s;
+            if (snp) snp[(long long)c * DV + col0 + j] = s;
         }
     }
     __syncthreads();
@@ -217,7 +225,7 @@ template <typename TI, typename TO, int D>
 cudaError_t launch_typed(const void* q, const void* k, const void* v,
                          const float* g, const float* beta, const float* S0,
                          const int32_t* cu, int32_t N, int64_t T_tot, int32_t H,
-                         void* o, float* S_final, const int32_t* ws,
+                         void* o, float* S_final, const int32_t* ws, const SnapArgs& snap,
                          cudaStream_t stream)
 {
     constexpr int DVS = D < 32 ? D : 32;
@@ -235,7 +243,7 @@ cudaError_t launch_typed(const void* q, const void* k, const void* v,
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     kern<<<(unsigned)blocks, kThreads, L::kBytes, stream>>>(
         static_cast<const TI*>(q), static_cast<const TI*>(k), static_cast<const TI*>(v),
-        g, beta, S0, cu, ws, (long long)T_tot, H, static_cast<TO*>(o), S_final);
+        g, beta, S0, cu, ws, (long long)T_tot, H, static_cast<TO*>(o), S_final, snap);
     return cudaGetLastError();
 }
 
@@ -243,14 +251,14 @@ template <typename TI, typename TO>
 cudaError_t launch_d(int32_t d, const void* q, const void* k, const void* v,
                      const float* g, const float* beta, const float* S0,
                      const int32_t* cu, int32_t N, int64_t T_tot, int32_t H,
-                     void* o, float* S_final, const int32_t* ws,
+                     void* o, float* S_final, const int32_t* ws, const SnapArgs& snap,
                      cudaStream_t stream)
 {
     switch (d) {
-        case 16: return launch_typed<TI, TO, 16>(q, k, v, g, beta, S0, cu, N, T_tot, H, o, S_final, ws, stream);
-        case 32: return launch_typed<TI, TO, 32>(q, k, v, g, beta, S0, cu, N, T_tot, H, o, S_final, ws, stream);
-        case 64: return launch_typed<TI, TO, 64>(q, k, v, g, beta, S0, cu, N, T_tot, H, o, S_final, ws, stream);
-        case 128: return launch_typed<TI, TO, 128>(q, k, v, g, beta, S0, cu, N, T_tot, H, o, S_final, ws, stream);
+        case 16: return launch_typed<TI, TO, 16>(q, k, v, g, beta, S0, cu, N, T_tot, H, o, S_final, ws, snap, stream);
+        case 32: return launch_typed<TI, TO, 32>(q, k, v, g, beta, S0, cu, N, T_tot, H, o, S_final, ws, snap, stream);
+        case 64: return launch_typed<TI, TO, 64>(q, k, v, g, beta, S0, cu, N, T_tot, H, o, S_final, ws, snap, stream);
+        case 128: return launch_typed<TI, TO, 128>(q, k, v, g, beta, S0, cu, N, T_tot, H, o, S_final, ws, snap, stream);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -262,19 +270,19 @@ cudaError_t launch_prefill_simt(const void* q, const void* k, const void* v,
                                 const float* S0, const int32_t* cu_seqlens,
                                 int32_t num_seqs, int64_t total_tokens, int32_t H,
                                 int32_t d, kda_dtype_t dtype, void* o,
-                                float* S_final, const int32_t* ws,
+                                float* S_final, const int32_t* ws, const SnapArgs& snap,
                                 cudaStream_t stream)
 {
     switch (dtype) {
         case KDA_BF16:
             return launch_d<__nv_bfloat16, __nv_bfloat16>(d, q, k, v, log_alpha, beta, S0, cu_seqlens,
-                                                          num_seqs, total_tokens, H, o, S_final, ws, stream);
+                                                          num_seqs, total_tokens, H, o, S_final, ws, snap, stream);
         case KDA_BF16_F32OUT:
             return launch_d<__nv_bfloat16, float>(d, q, k, v, log_alpha, beta, S0, cu_seqlens,
-                                                  num_seqs, total_tokens, H, o, S_final, ws, stream);
+                                                  num_seqs, total_tokens, H, o, S_final, ws, snap, stream);
         default:
             return launch_d<float, float>(d, q, k, v, log_alpha, beta, S0, cu_seqlens, num_seqs,
-                                          total_tokens, H, o, S_final, ws, stream);
+                                          total_tokens, H, o, S_final, ws, snap, stream);
     }
 }
 

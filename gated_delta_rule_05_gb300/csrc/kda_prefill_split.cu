@@ -131,7 +131,8 @@ __device__ __forceinline__ void consumer(const Ctx& X, uint32_t tmem, int warp, 
                                          const CUtensorMap* tm_v, const CUtensorMap* tm_o,
                                          const float* S0, const int32_t* cu, const int32_t* ws,
                                          long long total_tokens, int H, TO* o, float* S_final,
-                                         int U, int R, int32_t* flags, const uint8_t* ring)
+                                         int U, int R, int32_t* flags, const uint8_t* ring,
+                                         const SnapArgs& snap)
 {
     uint8_t* sm = X.sm;
     const int u = blockIdx.x;
@@ -232,6 +233,7 @@ __device__ __forceinline__ void consumer(const Ctx& X, uint32_t tmem, int warp, 
     } else {
         // ------------------------------------------------ compute group
         const Lane t = make_lane(threadIdx.x - 64, warp, lane);
+        const int seq_off = (cu != nullptr && snap.interval > 0) ? snap.offsets[n] : 0;
         state_load(t, tmem, S0, sbase);
         bool alive = nch > 0;
         StepDesc prev;
@@ -262,7 +264,9 @@ __device__ __forceinline__ void consumer(const Ctx& X, uint32_t tmem, int warp, 
             } else {
                 tc_fence_after();
             }
-            state_decay(t, tmem, reinterpret_cast<const float*>(sm + s * kStage + BLK_GL));
+            state_decay(t, tmem, reinterpret_cast<const float*>(sm + s * kStage + BLK_GL),
+                        d.first_pass ? snapshot_at(snap, d.chunk, eos - bos, seq_off, H, h)
+                                     : nullptr);
             fence_proxy_async_smem();             // the converted v tile
             tc_fence_before();
             if (t.ct == 0) bulk_wait_group_read0();   // the O staging is free again
@@ -289,8 +293,11 @@ __device__ __forceinline__ void consumer(const Ctx& X, uint32_t tmem, int warp, 
             store_prev_o(dd);
         }
         if (t.ct == 0) bulk_wait_group0();               // the last O store has landed
-        if (S_final && !*reinterpret_cast<volatile int32_t*>(&X.misc->abort))
-            state_store(t, tmem, S_final, sbase);
+        if (!*reinterpret_cast<volatile int32_t*>(&X.misc->abort)) {
+            if (S_final) state_store(t, tmem, S_final, sbase);
+            float* last = snapshot_at(snap, nch, eos - bos, seq_off, H, h);
+            if (last) state_store(t, tmem, last, 0);
+        }
     }
 }
 
@@ -515,7 +522,7 @@ prefill_split_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                      const __grid_constant__ CUtensorMap tm_o, const float* __restrict__ beta,
                      const float* S0, const int32_t* __restrict__ cu, int32_t* ws,
                      long long total_tokens, int H, TO* __restrict__ o, float* S_final, int U, int R,
-                     int32_t* flags, uint8_t* ring)
+                     int32_t* flags, uint8_t* ring, const SnapArgs snap)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -547,7 +554,7 @@ prefill_split_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
 
     if ((int)blockIdx.x < U)
         consumer<TO>(X, tmem, warp, lane, &tm_v, &tm_o, S0, cu, ws, total_tokens, H, o, S_final, U,
-                     R, flags, ring);
+                     R, flags, ring, snap);
     else
         producer(X, tmem, warp, lane, &tm_q, &tm_k, &tm_g, beta, cu, ws, total_tokens, H, U, R,
                  flags, ring);
@@ -564,7 +571,7 @@ template <typename TO>
 cudaError_t launch_typed(const void* q, const void* k, const void* v, const float* g,
                          const float* beta, const float* S0, const int32_t* cu, int64_t T,
                          int32_t H, void* o, float* S_final, int32_t* ws, const SplitPlan& plan,
-                         cudaStream_t stream)
+                         const SnapArgs& snap, cudaStream_t stream)
 {
     CUtensorMap mq, mk, mg, mv, mo;
     const bool bf16_out = sizeof(TO) == 2;
@@ -604,7 +611,7 @@ cudaError_t launch_typed(const void* q, const void* k, const void* v, const floa
     cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, kern, mq, mk, mg, mv, mo, beta, S0, cu, ws, (long long)T, (int)H,
                            static_cast<TO*>(o), S_final, (int)plan.units, (int)plan.ring, flags,
-                           ring);
+                           ring, snap);
     if (e != cudaSuccess && debug_enabled())
         fprintf(stderr, "kda: prefill_split launch failed: %s\n", cudaGetErrorString(e));
     return e;
@@ -617,14 +624,14 @@ cudaError_t launch_prefill_split(const void* q, const void* k, const void* v,
                                  const int32_t* cu_seqlens, int32_t num_seqs,
                                  int64_t total_tokens, int32_t H, kda_dtype_t dtype, void* o,
                                  float* S_final, int32_t* ws, const SplitPlan& plan,
-                                 cudaStream_t stream)
+                                 const SnapArgs& snap, cudaStream_t stream)
 {
     (void)num_seqs;
     if (dtype == KDA_BF16_F32OUT)
         return launch_typed<float>(q, k, v, log_alpha, beta, S0, cu_seqlens, total_tokens, H, o,
-                                   S_final, ws, plan, stream);
+                                   S_final, ws, plan, snap, stream);
     return launch_typed<__nv_bfloat16>(q, k, v, log_alpha, beta, S0, cu_seqlens, total_tokens, H,
-                                       o, S_final, ws, plan, stream);
+                                       o, S_final, ws, plan, snap, stream);
 }
 
 }  // namespace kda

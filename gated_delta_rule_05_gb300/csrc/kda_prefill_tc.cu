@@ -90,7 +90,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                   const __grid_constant__ CUtensorMap tm_o,
                   const float* __restrict__ beta, const float* S0,
                   const int32_t* __restrict__ cu, int32_t* ws, long long total_tokens, int H,
-                  TO* __restrict__ o, float* S_final)
+                  TO* __restrict__ o, float* S_final, const SnapArgs snap)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -205,6 +205,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         // -------------------------------------------------- compute group
         const Lane t = make_lane(tid - 64, warp, lane);
         const int ct = t.ct;
+        const int seq_off = (cu != nullptr && snap.interval > 0) ? snap.offsets[n] : 0;
         state_load(t, tmem, S0, sbase);
 
         int step = 0, chunk_v = 0;
@@ -250,7 +251,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 }
                 if (d.last_pass) ++chunk_v;
                 tc_fence_after();
-                state_decay(t, tmem, reinterpret_cast<const float*>(sm + OFF_GL));
+                state_decay(t, tmem, reinterpret_cast<const float*>(sm + OFF_GL),
+                            d.first_pass ? snapshot_at(snap, ch, eos - bos, seq_off, H, h) : nullptr);
                 fence_proxy_async_smem();                  // the converted v tile
                 tc_fence_before();
 
@@ -284,8 +286,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             }
         }
         if (ct == 0) bulk_wait_group0();                   // the last O store has landed
-        if (S_final && !*reinterpret_cast<volatile int32_t*>(&X.misc->abort))
-            state_store(t, tmem, S_final, sbase);
+        if (!*reinterpret_cast<volatile int32_t*>(&X.misc->abort)) {
+            if (S_final) state_store(t, tmem, S_final, sbase);
+            float* last = snapshot_at(snap, nch, eos - bos, seq_off, H, h);
+            if (last) state_store(t, tmem, last, 0);
+        }
     }
 
     tc_fence_before();
@@ -300,7 +305,7 @@ template <typename TO>
 cudaError_t launch_typed(const void* q, const void* k, const void* v, const float* g,
                          const float* beta, const float* S0, const int32_t* cu, int32_t N,
                          int64_t T, int32_t H, void* o, float* S_final, int32_t* ws,
-                         cudaStream_t stream)
+                         const SnapArgs& snap, cudaStream_t stream)
 {
     CUtensorMap mq, mk, mg, mv, mo;
     // The output map is used for bf16 output only (fp32 output is stored by
@@ -331,7 +336,7 @@ cudaError_t launch_typed(const void* q, const void* k, const void* v, const floa
     if (!bf16_out) mo = mq;
     kern<<<(unsigned)blocks, kThreads, kSmemBytes, stream>>>(mq, mk, mg, mv, mo, beta, S0, cu, ws,
                                                             (long long)T, H,
-                                                            static_cast<TO*>(o), S_final);
+                                                            static_cast<TO*>(o), S_final, snap);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess && debug_enabled())
         fprintf(stderr, "kda: prefill_tc launch failed: %s\n", cudaGetErrorString(e));
@@ -351,13 +356,13 @@ cudaError_t launch_prefill_tc(const void* q, const void* k, const void* v,
                               const float* log_alpha, const float* beta, const float* S0,
                               const int32_t* cu_seqlens, int32_t num_seqs, int64_t total_tokens,
                               int32_t H, kda_dtype_t dtype, void* o, float* S_final,
-                              int32_t* ws, cudaStream_t stream)
+                              int32_t* ws, const SnapArgs& snap, cudaStream_t stream)
 {
     if (dtype == KDA_BF16_F32OUT)
         return launch_typed<float>(q, k, v, log_alpha, beta, S0, cu_seqlens, num_seqs,
-                                   total_tokens, H, o, S_final, ws, stream);
+                                   total_tokens, H, o, S_final, ws, snap, stream);
     return launch_typed<__nv_bfloat16>(q, k, v, log_alpha, beta, S0, cu_seqlens, num_seqs,
-                                       total_tokens, H, o, S_final, ws, stream);
+                                       total_tokens, H, o, S_final, ws, snap, stream);
 }
 
 }  // namespace kda

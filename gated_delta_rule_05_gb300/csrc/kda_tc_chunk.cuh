@@ -731,9 +731,12 @@ __device__ __forceinline__ void v_tile_to_f16(uint8_t* vtile, int ct)
 }
 
 // State decay with its fp16 copy: S^T fp16 (the A operand of this step's
-// products) <- S^T, then S^T <- S^T Diag(e^{G_last}).  This thread: 64
-// channels of its TMEM lane.  No barrier.
-__device__ __forceinline__ void state_decay(const Lane& t, uint32_t tmem, const float* gl)
+// products) <- S^T, then S^T <- S^T Diag(e^{G_last}).  When `snap` is not
+// null the state before the decay (the state at this chunk's start) is also
+// stored there ([d_k][d_v] fp32).  This thread: 64 channels of its TMEM lane.
+// No barrier.
+__device__ __forceinline__ void state_decay(const Lane& t, uint32_t tmem, const float* gl,
+                                            float* snap = nullptr)
 {
 #pragma unroll
     for (int jb = 0; jb < 2; ++jb) {
@@ -741,6 +744,10 @@ __device__ __forceinline__ void state_decay(const Lane& t, uint32_t tmem, const 
         uint32_t r[32], b[16];
         tmem_ld32(tmem + t.lane_base + TM_S + c0, r);
         tmem_ld_wait();
+        if (snap != nullptr) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) snap[(long long)(c0 + i) * kD + t.L] = __uint_as_float(r[i]);
+        }
 #pragma unroll
         for (int i = 0; i < 16; ++i)
             b[i] = pack_f16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
@@ -823,6 +830,20 @@ __device__ __forceinline__ void state_load(const Lane& t, uint32_t tmem, const f
         tmem_st32(tmem + t.lane_base + TM_S + 64 * t.half + 32 * jb, r);
     }
     tmem_st_wait();
+}
+
+// Where the prefix snapshot taken at the start of chunk `ch` (the state after
+// the sequence's first 64 ch tokens) goes, or null when none is due there.
+// ch = the sequence's chunk count gives the end-of-sequence snapshot, due only
+// when 64 ch is the sequence's length `len`.
+__device__ __forceinline__ float* snapshot_at(const SnapArgs& sn, int ch, long long len, int seq_off,
+                                              int H, int h)
+{
+    if (sn.interval <= 0 || ch <= 0) return nullptr;
+    const long long tok = (long long)ch * kC;
+    if (tok > len || tok % sn.interval != 0) return nullptr;
+    const long long j = tok / sn.interval - 1;
+    return sn.out + ((long long)(seq_off + j) * H + h) * kD * kD;
 }
 
 __device__ __forceinline__ void state_store(const Lane& t, uint32_t tmem, float* S_final,

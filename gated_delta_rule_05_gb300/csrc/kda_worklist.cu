@@ -13,6 +13,8 @@
 //   * writes order[] = sequence indices sorted by length, longest first (ties
 //     by index), so that work items handed out in order approximate the
 //     longest-processing-time-first schedule;
+//   * checks the prefix-snapshot offsets when snapshots are requested
+//     (offsets[0] = 0, sequence n owning floor(len_n / interval) of them);
 //   * zeroes the hand-over flags of the split prefill kernel when it runs.
 // Without cu_seqlens (one sequence) only the counters, the length word and
 // the flags are written.
@@ -25,7 +27,8 @@ constexpr int kThreads = 1024;
 
 __global__ void __launch_bounds__(kThreads)
 worklist_kernel(const int32_t* __restrict__ cu, int32_t N, int64_t total_tokens,
-                int32_t* __restrict__ ws, int32_t* __restrict__ flags, int32_t nflags)
+                int32_t* __restrict__ ws, int32_t* __restrict__ flags, int32_t nflags,
+                int32_t snap_interval, const int32_t* __restrict__ snap_off)
 {
     __shared__ int bad;
     __shared__ int32_t maxlen;
@@ -45,12 +48,16 @@ worklist_kernel(const int32_t* __restrict__ cu, int32_t N, int64_t total_tokens,
     }
     if (tid == 0) {
         bad = (cu[0] != 0 || (int64_t)cu[N] != total_tokens) ? 1 : 0;
+        if (snap_off != nullptr && snap_off[0] != 0) bad = 1;
         maxlen = 0;
     }
     __syncthreads();
     for (int n = tid; n < N; n += kThreads) {
         const int32_t l = cu[n + 1] - cu[n];
         if (l < 0) atomicOr(&bad, 1);
+        // snapshot offsets: sequence n owns floor(len / interval) of them
+        if (snap_off != nullptr && l >= 0 && snap_off[n + 1] - snap_off[n] != l / snap_interval)
+            atomicOr(&bad, 1);
         atomicMax(&maxlen, l);
         if (N <= kMaxSortedSeqs) len[n] = l;
     }
@@ -82,10 +89,11 @@ worklist_kernel(const int32_t* __restrict__ cu, int32_t N, int64_t total_tokens,
 
 cudaError_t launch_worklist(const int32_t* cu_seqlens, int32_t num_seqs,
                             int64_t total_tokens, int32_t* ws, int32_t* flags,
-                            int32_t nflags, cudaStream_t stream)
+                            int32_t nflags, const SnapArgs& snap, cudaStream_t stream)
 {
+    const int32_t* off = (cu_seqlens != nullptr && snap.interval > 0) ? snap.offsets : nullptr;
     worklist_kernel<<<1, kThreads, 0, stream>>>(cu_seqlens, num_seqs, total_tokens, ws, flags,
-                                                nflags);
+                                                nflags, snap.interval, off);
     return cudaGetLastError();
 }
 

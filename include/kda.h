@@ -128,6 +128,37 @@ kda_status_t kda_prefill(const void *q, const void *k, const void *v,
                          float *S_final, void *workspace,
                          size_t workspace_bytes, cudaStream_t stream);
 
+/* kda_prefill that also records prefix states ("snapshots") for a prefix
+ * cache: the state of each sequence after every `interval` tokens, which a
+ * serving stack stores and later restores with S0 to resume from that prefix
+ * ("[논문 리뷰] Kimi K3 Technical Report", section 13, the KDA-aware prefix
+ * cache; "Kimi 모델 분석", section "요약본 저장 위치").
+ *
+ * Arguments, layouts and results are those of kda_prefill, plus:
+ *   interval      a positive multiple of 64 (so that every snapshot falls on
+ *                 a chunk boundary of every path); else KDA_ERR_INVALID_ARG.
+ *   snap_offsets  device int32 [N+1] with snap_offsets[0] = 0 and
+ *                 snap_offsets[n+1] - snap_offsets[n] = floor(len_n / interval);
+ *                 required when cu_seqlens is given, ignored (offset 0)
+ *                 otherwise.  Checked on the device: a mismatch is reported
+ *                 like an invalid cu_seqlens (workspace word at byte 4, nothing
+ *                 written).
+ *   snapshots     device fp32 [snap_offsets[N], H, d_k, d_v] (written).
+ *                 Snapshot j of sequence n, at snap_offsets[n] + j, is the
+ *                 state after that sequence's first (j + 1) * interval tokens;
+ *                 when interval divides the length, the last one equals the
+ *                 sequence's S_final.  Must not overlap the other buffers.
+ * The outputs o and S_final are those kda_prefill computes, bit for bit. */
+kda_status_t kda_prefill_snapshots(const void *q, const void *k, const void *v,
+                                   const float *log_alpha, const float *beta,
+                                   const float *S0, const int32_t *cu_seqlens,
+                                   int32_t num_seqs, int64_t total_tokens,
+                                   int32_t H, int32_t d_k, int32_t d_v,
+                                   kda_dtype_t dtype, void *o, float *S_final,
+                                   int32_t interval, const int32_t *snap_offsets,
+                                   float *snapshots, void *workspace,
+                                   size_t workspace_bytes, cudaStream_t stream);
+
 /* One decode step for N independent sequences (one new token each): the
  * recurrence above applied once per (sequence, head), state updated in place.
  * Decode reads and writes a fixed 2 * 4 * d_k * d_v bytes of fp32 state per
