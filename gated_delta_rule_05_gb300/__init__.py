@@ -9,6 +9,8 @@ Functions (same names as the C ABI):
   kda_prefill(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, ...)
   kda_prefill_snapshots(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, *, interval, ...)
   kda_decode_step(q, k, v, log_alpha, beta, S_inout, ...)
+  kda_decode_multi(q, k, v, log_alpha, beta, S_in, ...)
+  kda_state_gather(states, S_in, accept, ...)
   kda_prefill_workspace_bytes(num_seqs, H, d_k, d_v)
   kda_status_string(code)
 """
@@ -25,7 +27,8 @@ KDA_BF16, KDA_FP32, KDA_BF16_F32OUT = 0, 1, 2
 
 # Every symbol include/kda.h declares.
 EXPORTS = ("kda_prefill_workspace_bytes", "kda_prefill", "kda_decode_step",
-           "kda_status_string", "kda_prefill_noalloc", "kda_prefill_snapshots")
+           "kda_status_string", "kda_prefill_noalloc", "kda_prefill_snapshots",
+           "kda_decode_multi", "kda_state_gather")
 
 
 class KdaError(RuntimeError):
@@ -55,6 +58,11 @@ def _declare(lib):
                                     _i32, _i32, _i32, _i32, ctypes.c_int, _vp, _vp]
     lib.kda_status_string.restype = ctypes.c_char_p
     lib.kda_status_string.argtypes = [ctypes.c_int]
+    lib.kda_decode_multi.restype = ctypes.c_int
+    lib.kda_decode_multi.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
+                                     ctypes.c_int, _vp, _vp, _vp]
+    lib.kda_state_gather.restype = ctypes.c_int
+    lib.kda_state_gather.argtypes = [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp]
     lib.kda_prefill_snapshots.restype = ctypes.c_int
     lib.kda_prefill_snapshots.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                           _i32, _i64, _i32, _i32, _i32, ctypes.c_int,
@@ -306,3 +314,55 @@ def kda_prefill_snapshots(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, *,
     if rc != KDA_OK:
         raise KdaError(rc, "kda_prefill_snapshots")
     return o, S_final, snapshots, snap_offsets
+
+
+def kda_decode_multi(q, k, v, log_alpha, beta, S_in, *, o=None, states=None, stream=None,
+                     o_dtype=None):
+    """Ts decode tokens per sequence keeping every intermediate state
+    (C ABI: kda_decode_multi).  q, k, log_alpha: [N, Ts, H, d_k]; v:
+    [N, Ts, H, d_v]; beta: [N, Ts, H]; S_in: [N, H, d_k, d_v] (not modified).
+    Returns (o [N, Ts, H, d_v], states [N, Ts, H, d_k, d_v])."""
+    torch = _torch()
+    N, Ts, H, dk = q.shape
+    dv = v.shape[3]
+    if o_dtype is None:
+        o_dtype = o.dtype if o is not None else q.dtype
+    dt = _dtype_code(q, o_dtype)
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _check_cuda(name, t, q.dtype)
+    _check_cuda("log_alpha", log_alpha, torch.float32)
+    _check_cuda("beta", beta, torch.float32)
+    _check_cuda("S_in", S_in, torch.float32)
+    if o is None:
+        o = torch.empty((N, Ts, H, dv), dtype=o_dtype, device=q.device)
+    if states is None:
+        states = torch.empty((N, Ts, H, dk, dv), dtype=torch.float32, device=q.device)
+    _check_cuda("o", o, o_dtype)
+    _check_cuda("states", states, torch.float32)
+    with torch.cuda.device(q.device):
+        rc = lib().kda_decode_multi(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(S_in),
+            N, Ts, H, dk, dv, dt, _ptr(o), _ptr(states), _stream_handle(stream, q.device))
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_decode_multi")
+    return o, states
+
+
+def kda_state_gather(states, S_in, accept, *, S_out=None, stream=None):
+    """The state after each sequence's accepted prefix (C ABI:
+    kda_state_gather): S_out[n] = states[n, accept[n] - 1], or S_in[n] when
+    accept[n] is 0.  S_out may be S_in (in place).  Returns S_out."""
+    torch = _torch()
+    N, Ts, H, dk, dv = states.shape
+    _check_cuda("states", states, torch.float32)
+    _check_cuda("S_in", S_in, torch.float32)
+    _check_cuda("accept", accept, torch.int32)
+    if S_out is None:
+        S_out = torch.empty_like(S_in)
+    _check_cuda("S_out", S_out, torch.float32)
+    with torch.cuda.device(states.device):
+        rc = lib().kda_state_gather(_ptr(states), _ptr(S_in), _ptr(accept), N, Ts, H, dk, dv,
+                                    _ptr(S_out), _stream_handle(stream, states.device))
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_state_gather")
+    return S_out

@@ -191,6 +191,48 @@ kda_status_t kda_decode_step(const void* q, const void* k, const void* v,
     return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
+kda_status_t kda_decode_multi(const void* q, const void* k, const void* v,
+                              const float* log_alpha, const float* beta, const float* S_in,
+                              int32_t N, int32_t Ts, int32_t H, int32_t d_k, int32_t d_v,
+                              kda_dtype_t dtype, void* o, float* states, cudaStream_t stream)
+{
+    if (!valid_dtype(dtype)) return KDA_ERR_UNSUPPORTED;
+    if (d_k != d_v || !supported_d(d_k)) return KDA_ERR_UNSUPPORTED;
+    if (N < 1 || Ts < 1 || H < 1) return KDA_ERR_INVALID_ARG;
+    if (!q || !k || !v || !log_alpha || !beta || !S_in || !o || !states) return KDA_ERR_INVALID_ARG;
+    const void* ptrs16[] = {q, k, v, log_alpha, o, S_in, states};
+    for (const void* p : ptrs16)
+        if (!aligned(p, 16)) return KDA_ERR_INVALID_ARG;
+    if (!aligned(beta, 4)) return KDA_ERR_INVALID_ARG;
+    const size_t state_bytes = (size_t)N * H * d_k * d_v * sizeof(float);
+    const size_t states_bytes = state_bytes * Ts;
+    const size_t o_bytes = (size_t)N * Ts * H * d_v * out_bytes(dtype);
+    if (overlaps(states, states_bytes, S_in, state_bytes) || overlaps(states, states_bytes, o, o_bytes) ||
+        overlaps(o, o_bytes, S_in, state_bytes))
+        return KDA_ERR_INVALID_ARG;
+    cudaError_t err = kda::launch_decode_multi(q, k, v, log_alpha, beta, S_in, states, N, Ts, H,
+                                               d_k, dtype, o, stream);
+    return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+kda_status_t kda_state_gather(const float* states, const float* S_in, const int32_t* accept,
+                              int32_t N, int32_t Ts, int32_t H, int32_t d_k, int32_t d_v,
+                              float* S_out, cudaStream_t stream)
+{
+    if (d_k != d_v || !supported_d(d_k)) return KDA_ERR_UNSUPPORTED;
+    if (N < 1 || Ts < 1 || H < 1) return KDA_ERR_INVALID_ARG;
+    if (!states || !S_in || !accept || !S_out) return KDA_ERR_INVALID_ARG;
+    const void* ptrs16[] = {states, S_in, S_out};
+    for (const void* p : ptrs16)
+        if (!aligned(p, 16)) return KDA_ERR_INVALID_ARG;
+    if (!aligned(accept, 4)) return KDA_ERR_INVALID_ARG;
+    const size_t state_bytes = (size_t)N * H * d_k * d_v * sizeof(float);
+    if (overlaps(S_out, state_bytes, states, state_bytes * Ts)) return KDA_ERR_INVALID_ARG;
+    if (S_out != S_in && overlaps(S_out, state_bytes, S_in, state_bytes)) return KDA_ERR_INVALID_ARG;
+    cudaError_t err = kda::launch_state_gather(states, S_in, accept, N, Ts, H, d_k, d_v, S_out, stream);
+    return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
 const char* kda_status_string(kda_status_t status)
 {
     switch (status) {

@@ -14,6 +14,13 @@
 // once and written once, so one launch moves 8 * d_k * d_v bytes per
 // (sequence, head) plus a few hundred bytes of token inputs.
 //
+// Several tokens per sequence (the verification step of speculative decoding,
+// "[논문 리뷰] Kimi K3 Technical Report", section 13; "Kimi 모델 분석", section
+// "Dspark 투기적 디코딩"): the state is overwritten in place and cannot be
+// truncated, so the kernel keeps the state after every token.  It reads the
+// state once, applies Ts steps to it in registers and writes each step's state
+// to its own slot; the one-token decode is the case Ts = 1 written in place.
+//
 // Mapping: one CTA per (sequence, head, value-column slab).  Value columns of
 // S never mix (column j is updated with v_j alone), so a slab is independent.
 // Each thread holds R float4 of its slab in registers between the read and the
@@ -38,12 +45,16 @@ struct DecodeShape {
     static_assert(DVS <= THREADS && DK <= THREADS, "one thread per column / row");
 };
 
+// Token inputs are [N, Ts, H, .]; S_in is [N, H, d_k, d_v] and the state
+// after token t of (n, h) goes to S_out + ((n Ts + t) H + h) d_k d_v (for
+// Ts = 1 this is S_in's own layout, so the one-token decode passes
+// S_out = S_in).
 template <typename TI, typename TO, int DK, int DVS, int THREADS>
 __global__ void __launch_bounds__(THREADS)
 decode_kernel(const TI* __restrict__ q, const TI* __restrict__ k,
               const TI* __restrict__ v, const float* __restrict__ log_alpha,
-              const float* __restrict__ beta, float* __restrict__ S,
-              TO* __restrict__ o, int dv)
+              const float* __restrict__ beta, const float* S_in, float* S_out,
+              TO* __restrict__ o, int dv, int Ts, int H)
 {
     using Sh = DecodeShape<DK, DVS, THREADS>;
     constexpr int LPR = Sh::kLanesPerRow;
@@ -58,8 +69,9 @@ decode_kernel(const TI* __restrict__ q, const TI* __restrict__ k,
     const int c4 = tid % LPR;                     // float4 column within the slab
     const int rg = tid / LPR;                     // first row of this thread
     const int col = slab * DVS + c4 * 4;
+    const long long n = nh / H, h = nh % H;
 
-    float* Sp = S + nh * (long long)DK * dv;
+    const float* Sp = S_in + nh * (long long)DK * dv;
 
     // 1. Issue every state load first so that they are all in flight.
     float4 s[R];
@@ -75,92 +87,118 @@ decode_kernel(const TI* __restrict__ q, const TI* __restrict__ k,
     __shared__ float sh_kq[Sh::kWarps];
     __shared__ float sh_u[DVS];
 
-    // 2. Token inputs: alpha, k, alpha.*k, alpha.*q and the partial k.q.
-    float kq = 0.f;
-    if (tid < DK) {
-        const long long off = nh * DK + tid;
-        const float a = expf(log_alpha[off]);
-        const float kk = ld_f(k + off);
-        const float qq = ld_f(q + off);
-        sh_a[tid] = a;
-        sh_k[tid] = kk;
-        sh_ak[tid] = a * kk;
-        sh_aq[tid] = a * qq;
-        kq = kk * qq;
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, off);
-    if (lane == 0) sh_kq[warp] = kq;
-    __syncthreads();
+    for (int t = 0; t < Ts; ++t) {
+        const long long tok = (n * Ts + t) * H + h;       // token row of this (n, t, h)
+        float* Sq = S_out + tok * (long long)DK * dv;
+        if (t > 0) __syncthreads();                        // the previous token's reads are done
 
-    // 3. Partial column sums of S^T(alpha.*k) and S^T(alpha.*q) over this
-    //    thread's rows, then across lanes that share the same columns.
-    float4 w = make_float4(0.f, 0.f, 0.f, 0.f), p = w;
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-        const int i = rg + r * RPP;
-        const float ak = sh_ak[i], aq = sh_aq[i];
-        w.x = fmaf(ak, s[r].x, w.x); w.y = fmaf(ak, s[r].y, w.y);
-        w.z = fmaf(ak, s[r].z, w.z); w.w = fmaf(ak, s[r].w, w.w);
-        p.x = fmaf(aq, s[r].x, p.x); p.y = fmaf(aq, s[r].y, p.y);
-        p.z = fmaf(aq, s[r].z, p.z); p.w = fmaf(aq, s[r].w, p.w);
-    }
-#pragma unroll
-    for (int off = LPR; off < 32; off <<= 1) {
-        w.x += __shfl_xor_sync(0xffffffffu, w.x, off);
-        w.y += __shfl_xor_sync(0xffffffffu, w.y, off);
-        w.z += __shfl_xor_sync(0xffffffffu, w.z, off);
-        w.w += __shfl_xor_sync(0xffffffffu, w.w, off);
-        p.x += __shfl_xor_sync(0xffffffffu, p.x, off);
-        p.y += __shfl_xor_sync(0xffffffffu, p.y, off);
-        p.z += __shfl_xor_sync(0xffffffffu, p.z, off);
-        p.w += __shfl_xor_sync(0xffffffffu, p.w, off);
-    }
-    if (lane < LPR) {
-        sh_red_w[warp][c4 * 4 + 0] = w.x; sh_red_w[warp][c4 * 4 + 1] = w.y;
-        sh_red_w[warp][c4 * 4 + 2] = w.z; sh_red_w[warp][c4 * 4 + 3] = w.w;
-        sh_red_p[warp][c4 * 4 + 0] = p.x; sh_red_p[warp][c4 * 4 + 1] = p.y;
-        sh_red_p[warp][c4 * 4 + 2] = p.z; sh_red_p[warp][c4 * 4 + 3] = p.w;
-    }
-    __syncthreads();
-
-    // 4. Per value column: u = beta (v - w), o = p + (k.q) u.
-    if (tid < DVS) {
-        float ws = 0.f, ps = 0.f, kqs = 0.f;
-#pragma unroll
-        for (int i = 0; i < Sh::kWarps; ++i) {
-            ws += sh_red_w[i][tid];
-            ps += sh_red_p[i][tid];
-            kqs += sh_kq[i];
+        // 2. Token inputs: alpha, k, alpha.*k, alpha.*q and the partial k.q.
+        float kq = 0.f;
+        if (tid < DK) {
+            const long long off = tok * DK + tid;
+            const float a = expf(log_alpha[off]);
+            const float kk = ld_f(k + off);
+            const float qq = ld_f(q + off);
+            sh_a[tid] = a;
+            sh_k[tid] = kk;
+            sh_ak[tid] = a * kk;
+            sh_aq[tid] = a * qq;
+            kq = kk * qq;
         }
-        const int j = slab * DVS + tid;
-        const long long vo = nh * dv + j;
-        const float u = beta[nh] * (ld_f(v + vo) - ws);
-        st_f(o + vo, fmaf(kqs, u, ps));
-        sh_u[tid] = u;
-    }
-    __syncthreads();
-
-    // 5. S' = Diag(alpha) S + k u^T, streamed back.
-    const float4 u4 = make_float4(sh_u[c4 * 4 + 0], sh_u[c4 * 4 + 1],
-                                  sh_u[c4 * 4 + 2], sh_u[c4 * 4 + 3]);
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
-        const int i = rg + r * RPP;
-        const float a = sh_a[i], kk = sh_k[i];
-        float4 x;
-        x.x = fmaf(a, s[r].x, kk * u4.x);
-        x.y = fmaf(a, s[r].y, kk * u4.y);
-        x.z = fmaf(a, s[r].z, kk * u4.z);
-        x.w = fmaf(a, s[r].w, kk * u4.w);
-        __stcs(reinterpret_cast<float4*>(Sp + (long long)i * dv + col), x);
+        for (int off = 16; off > 0; off >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, off);
+        if (lane == 0) sh_kq[warp] = kq;
+        __syncthreads();
+
+        // 3. Partial column sums of S^T(alpha.*k) and S^T(alpha.*q) over this
+        //    thread's rows, then across lanes that share the same columns.
+        float4 w = make_float4(0.f, 0.f, 0.f, 0.f), p = w;
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const int i = rg + r * RPP;
+            const float ak = sh_ak[i], aq = sh_aq[i];
+            w.x = fmaf(ak, s[r].x, w.x); w.y = fmaf(ak, s[r].y, w.y);
+            w.z = fmaf(ak, s[r].z, w.z); w.w = fmaf(ak, s[r].w, w.w);
+            p.x = fmaf(aq, s[r].x, p.x); p.y = fmaf(aq, s[r].y, p.y);
+            p.z = fmaf(aq, s[r].z, p.z); p.w = fmaf(aq, s[r].w, p.w);
+        }
+#pragma unroll
+        for (int off = LPR; off < 32; off <<= 1) {
+            w.x += __shfl_xor_sync(0xffffffffu, w.x, off);
+            w.y += __shfl_xor_sync(0xffffffffu, w.y, off);
+            w.z += __shfl_xor_sync(0xffffffffu, w.z, off);
+            w.w += __shfl_xor_sync(0xffffffffu, w.w, off);
+            p.x += __shfl_xor_sync(0xffffffffu, p.x, off);
+            p.y += __shfl_xor_sync(0xffffffffu, p.y, off);
+            p.z += __shfl_xor_sync(0xffffffffu, p.z, off);
+            p.w += __shfl_xor_sync(0xffffffffu, p.w, off);
+        }
+        if (lane < LPR) {
+            sh_red_w[warp][c4 * 4 + 0] = w.x; sh_red_w[warp][c4 * 4 + 1] = w.y;
+            sh_red_w[warp][c4 * 4 + 2] = w.z; sh_red_w[warp][c4 * 4 + 3] = w.w;
+            sh_red_p[warp][c4 * 4 + 0] = p.x; sh_red_p[warp][c4 * 4 + 1] = p.y;
+            sh_red_p[warp][c4 * 4 + 2] = p.z; sh_red_p[warp][c4 * 4 + 3] = p.w;
+        }
+        __syncthreads();
+
+        // 4. Per value column: u = beta (v - w), o = p + (k.q) u.
+        if (tid < DVS) {
+            float ws = 0.f, ps = 0.f, kqs = 0.f;
+#pragma unroll
+            for (int i = 0; i < Sh::kWarps; ++i) {
+                ws += sh_red_w[i][tid];
+                ps += sh_red_p[i][tid];
+                kqs += sh_kq[i];
+            }
+            const int j = slab * DVS + tid;
+            const long long vo = tok * dv + j;
+            const float u = beta[tok] * (ld_f(v + vo) - ws);
+            st_f(o + vo, fmaf(kqs, u, ps));
+            sh_u[tid] = u;
+        }
+        __syncthreads();
+
+        // 5. S' = Diag(alpha) S + k u^T, streamed out; kept for the next token.
+        const float4 u4 = make_float4(sh_u[c4 * 4 + 0], sh_u[c4 * 4 + 1],
+                                      sh_u[c4 * 4 + 2], sh_u[c4 * 4 + 3]);
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const int i = rg + r * RPP;
+            const float a = sh_a[i], kk = sh_k[i];
+            float4 x;
+            x.x = fmaf(a, s[r].x, kk * u4.x);
+            x.y = fmaf(a, s[r].y, kk * u4.y);
+            x.z = fmaf(a, s[r].z, kk * u4.z);
+            x.w = fmaf(a, s[r].w, kk * u4.w);
+            __stcs(reinterpret_cast<float4*>(Sq + (long long)i * dv + col), x);
+            s[r] = x;
+        }
     }
+}
+
+// The state after the accepted prefix of a multi-token step: for each
+// (sequence, head), states[n, accept[n] - 1] when accept[n] > 0, else S_in[n]
+// (accept values are clamped to [0, Ts]).  One CTA per (sequence, head).
+__global__ void __launch_bounds__(256)
+state_gather_kernel(const float* __restrict__ states, const float* S_in,
+                    const int32_t* __restrict__ accept, float* S_out, int Ts, int H,
+                    long long elems)
+{
+    const long long nh = blockIdx.x;
+    const long long n = nh / H, h = nh % H;
+    int a = accept[n];
+    a = a < 0 ? 0 : (a > Ts ? Ts : a);
+    const float4* src = reinterpret_cast<const float4*>(
+        a > 0 ? states + ((n * Ts + (a - 1)) * H + h) * elems : S_in + nh * elems);
+    float4* dst = reinterpret_cast<float4*>(S_out + nh * elems);
+    if (reinterpret_cast<const void*>(src) == reinterpret_cast<const void*>(dst)) return;
+    for (long long i = threadIdx.x; i < elems / 4; i += blockDim.x) dst[i] = __ldcs(src + i);
 }
 
 template <typename TI, typename TO, int D>
 cudaError_t launch_typed(const void* q, const void* k, const void* v,
-                         const float* g, const float* beta, float* S,
-                         int32_t N, int32_t H, void* o, cudaStream_t stream)
+                         const float* g, const float* beta, const float* S_in, float* S_out,
+                         int32_t N, int32_t Ts, int32_t H, void* o, cudaStream_t stream)
 {
     // Slab widths and thread counts: 32 KiB of state per CTA at d = 128
     // (8 float4 per thread), one warp-row pattern per smaller head size.
@@ -171,21 +209,39 @@ cudaError_t launch_typed(const void* q, const void* k, const void* v,
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     decode_kernel<TI, TO, D, DVS, THREADS><<<(unsigned)blocks, THREADS, 0, stream>>>(
         static_cast<const TI*>(q), static_cast<const TI*>(k), static_cast<const TI*>(v),
-        g, beta, S, static_cast<TO*>(o), D);
+        g, beta, S_in, S_out, static_cast<TO*>(o), D, Ts, H);
     return cudaGetLastError();
 }
 
 template <typename TI, typename TO>
 cudaError_t launch_d(int32_t d, const void* q, const void* k, const void* v,
-                     const float* g, const float* beta, float* S, int32_t N,
-                     int32_t H, void* o, cudaStream_t stream)
+                     const float* g, const float* beta, const float* S_in, float* S_out,
+                     int32_t N, int32_t Ts, int32_t H, void* o, cudaStream_t stream)
 {
     switch (d) {
-        case 16: return launch_typed<TI, TO, 16>(q, k, v, g, beta, S, N, H, o, stream);
-        case 32: return launch_typed<TI, TO, 32>(q, k, v, g, beta, S, N, H, o, stream);
-        case 64: return launch_typed<TI, TO, 64>(q, k, v, g, beta, S, N, H, o, stream);
-        case 128: return launch_typed<TI, TO, 128>(q, k, v, g, beta, S, N, H, o, stream);
+        case 16: return launch_typed<TI, TO, 16>(q, k, v, g, beta, S_in, S_out, N, Ts, H, o, stream);
+        case 32: return launch_typed<TI, TO, 32>(q, k, v, g, beta, S_in, S_out, N, Ts, H, o, stream);
+        case 64: return launch_typed<TI, TO, 64>(q, k, v, g, beta, S_in, S_out, N, Ts, H, o, stream);
+        case 128: return launch_typed<TI, TO, 128>(q, k, v, g, beta, S_in, S_out, N, Ts, H, o, stream);
         default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_multi(const void* q, const void* k, const void* v, const float* log_alpha,
+                         const float* beta, const float* S_in, float* S_out, int32_t N,
+                         int32_t Ts, int32_t H, int32_t d, kda_dtype_t dtype, void* o,
+                         cudaStream_t stream)
+{
+    switch (dtype) {
+        case KDA_BF16:
+            return launch_d<__nv_bfloat16, __nv_bfloat16>(d, q, k, v, log_alpha, beta, S_in, S_out,
+                                                          N, Ts, H, o, stream);
+        case KDA_BF16_F32OUT:
+            return launch_d<__nv_bfloat16, float>(d, q, k, v, log_alpha, beta, S_in, S_out, N, Ts,
+                                                  H, o, stream);
+        default:
+            return launch_d<float, float>(d, q, k, v, log_alpha, beta, S_in, S_out, N, Ts, H, o,
+                                          stream);
     }
 }
 
@@ -196,14 +252,27 @@ cudaError_t launch_decode(const void* q, const void* k, const void* v,
                           int32_t N, int32_t H, int32_t d, kda_dtype_t dtype,
                           void* o, cudaStream_t stream)
 {
-    switch (dtype) {
-        case KDA_BF16:
-            return launch_d<__nv_bfloat16, __nv_bfloat16>(d, q, k, v, log_alpha, beta, S, N, H, o, stream);
-        case KDA_BF16_F32OUT:
-            return launch_d<__nv_bfloat16, float>(d, q, k, v, log_alpha, beta, S, N, H, o, stream);
-        default:
-            return launch_d<float, float>(d, q, k, v, log_alpha, beta, S, N, H, o, stream);
-    }
+    return launch_multi(q, k, v, log_alpha, beta, S, S, N, 1, H, d, dtype, o, stream);
+}
+
+cudaError_t launch_decode_multi(const void* q, const void* k, const void* v,
+                                const float* log_alpha, const float* beta, const float* S_in,
+                                float* states, int32_t N, int32_t Ts, int32_t H, int32_t d,
+                                kda_dtype_t dtype, void* o, cudaStream_t stream)
+{
+    return launch_multi(q, k, v, log_alpha, beta, S_in, states, N, Ts, H, d, dtype, o, stream);
+}
+
+cudaError_t launch_state_gather(const float* states, const float* S_in, const int32_t* accept,
+                                int32_t N, int32_t Ts, int32_t H, int32_t d_k, int32_t d_v,
+                                float* S_out, cudaStream_t stream)
+{
+    const long long blocks = (long long)N * H;
+    if (blocks <= 0) return cudaSuccess;
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    state_gather_kernel<<<(unsigned)blocks, 256, 0, stream>>>(states, S_in, accept, S_out, Ts, H,
+                                                              (long long)d_k * d_v);
+    return cudaGetLastError();
 }
 
 }  // namespace kda

@@ -114,6 +114,17 @@ cudaError_t launch_decode(const void* q, const void* k, const void* v,
                           int32_t N, int32_t H, int32_t d, kda_dtype_t dtype,
                           void* o, cudaStream_t stream);
 
+// Ts tokens per sequence from S_in, the state after each token to `states`
+// ([N, Ts, H, d, d]); the one-token decode above is the case Ts = 1 in place.
+cudaError_t launch_decode_multi(const void* q, const void* k, const void* v,
+                                const float* log_alpha, const float* beta, const float* S_in,
+                                float* states, int32_t N, int32_t Ts, int32_t H, int32_t d,
+                                kda_dtype_t dtype, void* o, cudaStream_t stream);
+
+cudaError_t launch_state_gather(const float* states, const float* S_in, const int32_t* accept,
+                                int32_t N, int32_t Ts, int32_t H, int32_t d_k, int32_t d_v,
+                                float* S_out, cudaStream_t stream);
+
 cudaError_t launch_prefill_simt(const void* q, const void* k, const void* v,
                                 const float* log_alpha, const float* beta,
                                 const float* S0, const int32_t* cu_seqlens,

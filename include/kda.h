@@ -177,6 +177,40 @@ kda_status_t kda_decode_step(const void *q, const void *k, const void *v,
                              int32_t d_v, kda_dtype_t dtype, void *o,
                              cudaStream_t stream);
 
+/* Several decode tokens per sequence, keeping the state after every token:
+ * the verification step of speculative decoding, which must be able to
+ * return to the state after any accepted prefix of the draft, since the state
+ * is overwritten in place and cannot be truncated ("[논문 리뷰] Kimi K3
+ * Technical Report", section 13, speculative decoding replay; "Kimi 모델
+ * 분석", section "Dspark 투기적 디코딩").  Token t of each sequence is one
+ * decode step (the recurrence above) from the state after token t - 1.
+ *
+ *   q, k, log_alpha [N, Ts, H, d_k]; v [N, Ts, H, d_v]; beta [N, Ts, H]
+ *                   in the dtypes of kda_decode_step
+ *   S_in            [N, H, d_k, d_v] fp32, the state before the first token
+ *                   (read only)
+ *   o               [N, Ts, H, d_v] in the output dtype (written)
+ *   states          [N, Ts, H, d_k, d_v] fp32: states[n, t] is the state after
+ *                   token t of sequence n (written)
+ * No two of S_in, o and states may overlap.  The launch reads S_in once and
+ * writes Ts states: 4 (1 + Ts) d_k d_v bytes per (sequence, head). */
+kda_status_t kda_decode_multi(const void *q, const void *k, const void *v,
+                              const float *log_alpha, const float *beta,
+                              const float *S_in, int32_t N, int32_t Ts,
+                              int32_t H, int32_t d_k, int32_t d_v,
+                              kda_dtype_t dtype, void *o, float *states,
+                              cudaStream_t stream);
+
+/* After verification: the state of each sequence after its accepted prefix.
+ * S_out[n] = states[n, accept[n] - 1] when accept[n] > 0, else S_in[n]
+ * (all heads).  accept: device int32 [N] in [0, Ts] (values outside are
+ * clamped).  S_out may be S_in itself (in-place update of the cache) and must
+ * not overlap `states`. */
+kda_status_t kda_state_gather(const float *states, const float *S_in,
+                              const int32_t *accept, int32_t N, int32_t Ts,
+                              int32_t H, int32_t d_k, int32_t d_v, float *S_out,
+                              cudaStream_t stream);
+
 /* kda_prefill for callers that cannot allocate device memory.
  *
  * The pages have no counterpart to this entry point: it exists for callers
