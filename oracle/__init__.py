@@ -215,3 +215,24 @@ def decode_multi(q, k, v, log_alpha, beta, S, nthreads: int | None = None, lib=N
                                    nthreads=nthreads, lib=lib)
         states[:, t] = cur
     return o, states
+
+
+G_MIN = -5.0
+
+
+def gate_prologue(q, k, z, A, q_scale: float):
+    """The steps in front of the recurrence, in float64: the lower-bounded
+    log-decay g = g_min * sigmoid(e^A z) with g_min = -5 ("[논문 리뷰] Kimi K3
+    Technical Report", section 3.5, so that g lies in (-5, 0) and
+    alpha = exp(g) in (e^-5, 1)), and the L2 normalisation of q and k over
+    the key channels, q also multiplied by q_scale.
+
+    q, k, z: [..., H, d_k]; A: [H, d_k] (one value per head and key channel;
+    a per-head A is the same value repeated over the channels).
+    Returns (q_hat, k_hat, g)."""
+    q, k, z, A = (_c64(x) for x in (q, k, z, A))
+    s = np.exp(A) * z
+    g = G_MIN / (1.0 + np.exp(-s))
+    qn = np.sqrt(np.sum(q * q, axis=-1, keepdims=True))
+    kn = np.sqrt(np.sum(k * k, axis=-1, keepdims=True))
+    return q * (float(q_scale) / qn), k / kn, g
