@@ -232,7 +232,7 @@ def gate_prologue(q, k, z, A, q_scale: float):
     Returns (q_hat, k_hat, g)."""
     q, k, z, A = (_c64(x) for x in (q, k, z, A))
     s = np.exp(A) * z
-    g = G_MIN / (1.0 + np.exp(-s))
+    g = G_MIN * 0.5 * (1.0 + np.tanh(0.5 * s))     # sigmoid(s), without overflow
     qn = np.sqrt(np.sum(q * q, axis=-1, keepdims=True))
     kn = np.sqrt(np.sum(k * k, axis=-1, keepdims=True))
     return q * (float(q_scale) / qn), k / kn, g
