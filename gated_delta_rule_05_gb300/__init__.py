@@ -10,6 +10,8 @@ Functions (same names as the C ABI):
   kda_prefill_snapshots(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, *, interval, ...)
   kda_decode_step(q, k, v, log_alpha, beta, S_inout, ...)
   kda_decode_multi(q, k, v, log_alpha, beta, S_in, ...)
+  kda_prefill_fused(q, k, v, z, A, beta, ..., q_scale)
+  kda_decode_step_fused(q, k, v, z, A, beta, S_inout, ..., q_scale)
   kda_state_gather(states, S_in, accept, ...)
   kda_prefill_workspace_bytes(num_seqs, H, d_k, d_v)
   kda_status_string(code)
@@ -28,7 +30,8 @@ KDA_BF16, KDA_FP32, KDA_BF16_F32OUT = 0, 1, 2
 # Every symbol include/kda.h declares.
 EXPORTS = ("kda_prefill_workspace_bytes", "kda_prefill", "kda_decode_step",
            "kda_status_string", "kda_prefill_noalloc", "kda_prefill_snapshots",
-           "kda_decode_multi", "kda_state_gather")
+           "kda_decode_multi", "kda_state_gather", "kda_prefill_fused",
+           "kda_decode_step_fused")
 
 
 class KdaError(RuntimeError):
@@ -58,6 +61,13 @@ def _declare(lib):
                                     _i32, _i32, _i32, _i32, ctypes.c_int, _vp, _vp]
     lib.kda_status_string.restype = ctypes.c_char_p
     lib.kda_status_string.argtypes = [ctypes.c_int]
+    lib.kda_prefill_fused.restype = ctypes.c_int
+    lib.kda_prefill_fused.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                      _i32, _i64, _i32, _i32, _i32, ctypes.c_int, ctypes.c_float,
+                                      _vp, _vp, _vp, _sz, _vp]
+    lib.kda_decode_step_fused.restype = ctypes.c_int
+    lib.kda_decode_step_fused.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32,
+                                          _i32, ctypes.c_int, ctypes.c_float, _vp, _vp]
     lib.kda_decode_multi.restype = ctypes.c_int
     lib.kda_decode_multi.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
                                      ctypes.c_int, _vp, _vp, _vp]
@@ -366,3 +376,73 @@ def kda_state_gather(states, S_in, accept, *, S_out=None, stream=None):
     if rc != KDA_OK:
         raise KdaError(rc, "kda_state_gather")
     return S_out
+
+
+def kda_prefill_fused(q, k, v, z, A, beta, S0=None, cu_seqlens=None, *, q_scale, o=None,
+                      S_final=None, want_state=True, workspace=None, stream=None, o_dtype=None):
+    """kda_prefill with the gate prologue in the kernels (C ABI:
+    kda_prefill_fused): raw q, k (L2-normalised inside, q times q_scale), the
+    gate pre-activation z [T, H, d_k] and A [H, d_k] (g = -5 sigmoid(e^A z)).
+    Returns (o, S_final)."""
+    torch = _torch()
+    T, H, dk = q.shape
+    dv = v.shape[2]
+    if o_dtype is None:
+        o_dtype = o.dtype if o is not None else q.dtype
+    dt = _dtype_code(q, o_dtype)
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _check_cuda(name, t, q.dtype)
+    _check_cuda("z", z, torch.float32)
+    _check_cuda("A", A, torch.float32)
+    _check_cuda("beta", beta, torch.float32)
+    _check_cuda("S0", S0, torch.float32)
+    _check_cuda("cu_seqlens", cu_seqlens, torch.int32)
+    N = 1 if cu_seqlens is None else cu_seqlens.shape[0] - 1
+    dev = q.device
+    if o is None:
+        o = torch.empty((T, H, dv), dtype=o_dtype, device=dev)
+    _check_cuda("o", o, o_dtype)
+    if S_final is None and want_state:
+        S_final = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
+    _check_cuda("S_final", S_final, torch.float32)
+    need = kda_prefill_workspace_bytes(N, H, dk, dv)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    _check_cuda("workspace", workspace)
+    with torch.cuda.device(dev):
+        rc = lib().kda_prefill_fused(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(A), _ptr(beta), _ptr(S0),
+            _ptr(cu_seqlens), N, T, H, dk, dv, dt, float(q_scale), _ptr(o), _ptr(S_final),
+            _ptr(workspace), workspace.numel() * workspace.element_size(),
+            _stream_handle(stream, dev))
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_prefill_fused")
+    return o, S_final
+
+
+def kda_decode_step_fused(q, k, v, z, A, beta, S_inout, *, q_scale, o=None, stream=None,
+                          o_dtype=None):
+    """kda_decode_step with the gate prologue in the kernel (C ABI:
+    kda_decode_step_fused).  Returns o; S_inout is updated in place."""
+    torch = _torch()
+    N, H, dk = q.shape
+    dv = v.shape[2]
+    if o_dtype is None:
+        o_dtype = o.dtype if o is not None else q.dtype
+    dt = _dtype_code(q, o_dtype)
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _check_cuda(name, t, q.dtype)
+    _check_cuda("z", z, torch.float32)
+    _check_cuda("A", A, torch.float32)
+    _check_cuda("beta", beta, torch.float32)
+    _check_cuda("S_inout", S_inout, torch.float32)
+    if o is None:
+        o = torch.empty((N, H, dv), dtype=o_dtype, device=q.device)
+    _check_cuda("o", o, o_dtype)
+    with torch.cuda.device(q.device):
+        rc = lib().kda_decode_step_fused(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(A), _ptr(beta), _ptr(S_inout),
+            N, H, dk, dv, dt, float(q_scale), _ptr(o), _stream_handle(stream, q.device))
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_decode_step_fused")
+    return o

@@ -65,8 +65,8 @@ kda_status_t prefill_impl(const void* q, const void* k, const void* v, const flo
                           const float* beta, const float* S0, const int32_t* cu_seqlens,
                           int32_t num_seqs, int64_t total_tokens, int32_t H, int32_t d_k,
                           int32_t d_v, kda_dtype_t dtype, void* o, float* S_final,
-                          const kda::SnapArgs& snap, void* workspace, size_t workspace_bytes,
-                          cudaStream_t stream)
+                          const kda::SnapArgs& snap, const kda::GateArgs& gate, void* workspace,
+                          size_t workspace_bytes, cudaStream_t stream)
 {
     if (!valid_dtype(dtype)) return KDA_ERR_UNSUPPORTED;
     if (d_k != d_v || !supported_d(d_k)) return KDA_ERR_UNSUPPORTED;
@@ -76,6 +76,7 @@ kda_status_t prefill_impl(const void* q, const void* k, const void* v, const flo
     if (total_tokens > INT32_MAX) return KDA_ERR_INVALID_ARG;
     if (total_tokens > 0 && (!q || !k || !v || !log_alpha || !beta || !o))
         return KDA_ERR_INVALID_ARG;
+    if (gate.A && !aligned(gate.A, 16)) return KDA_ERR_INVALID_ARG;
     const void* ptrs16[] = {q, k, v, log_alpha, o, S0, S_final, snap.out};
     for (const void* p : ptrs16)
         if (p && !aligned(p, 16)) return KDA_ERR_INVALID_ARG;
@@ -110,7 +111,8 @@ kda_status_t prefill_impl(const void* q, const void* k, const void* v, const flo
     }
     if (split) {
         err = kda::launch_prefill_split(q, k, v, log_alpha, beta, S0, cu_seqlens, num_seqs,
-                                        total_tokens, H, dtype, o, S_final, ws, plan, snap, stream);
+                                        total_tokens, H, dtype, o, S_final, ws, plan, snap, gate,
+                                        stream);
         if (err == cudaSuccess) return KDA_OK;
         // The launch was refused (a configuration error, nothing ran): the
         // single-CTA kernel computes the same result.
@@ -118,10 +120,11 @@ kda_status_t prefill_impl(const void* q, const void* k, const void* v, const flo
     }
     if (tc)
         err = kda::launch_prefill_tc(q, k, v, log_alpha, beta, S0, cu_seqlens, num_seqs,
-                                     total_tokens, H, dtype, o, S_final, ws, snap, stream);
+                                     total_tokens, H, dtype, o, S_final, ws, snap, gate, stream);
     else
         err = kda::launch_prefill_simt(q, k, v, log_alpha, beta, S0, cu_seqlens, num_seqs,
-                                       total_tokens, H, d_k, dtype, o, S_final, ws, snap, stream);
+                                       total_tokens, H, d_k, dtype, o, S_final, ws, snap, gate,
+                                       stream);
     return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
@@ -138,8 +141,9 @@ kda_status_t kda_prefill(const void* q, const void* k, const void* v,
                          cudaStream_t stream)
 {
     const kda::SnapArgs none{0, nullptr, nullptr};
+    const kda::GateArgs given{nullptr, 1.f};
     return prefill_impl(q, k, v, log_alpha, beta, S0, cu_seqlens, num_seqs, total_tokens, H, d_k,
-                        d_v, dtype, o, S_final, none, workspace, workspace_bytes, stream);
+                        d_v, dtype, o, S_final, none, given, workspace, workspace_bytes, stream);
 }
 
 kda_status_t kda_prefill_snapshots(const void* q, const void* k, const void* v,
@@ -165,8 +169,23 @@ kda_status_t kda_prefill_snapshots(const void* q, const void* k, const void* v,
             return KDA_ERR_INVALID_ARG;
     }
     const kda::SnapArgs snap{interval, cu_seqlens ? snap_offsets : nullptr, snapshots};
+    const kda::GateArgs given{nullptr, 1.f};
     return prefill_impl(q, k, v, log_alpha, beta, S0, cu_seqlens, num_seqs, total_tokens, H, d_k,
-                        d_v, dtype, o, S_final, snap, workspace, workspace_bytes, stream);
+                        d_v, dtype, o, S_final, snap, given, workspace, workspace_bytes, stream);
+}
+
+kda_status_t kda_prefill_fused(const void* q, const void* k, const void* v, const float* z,
+                               const float* A, const float* beta, const float* S0,
+                               const int32_t* cu_seqlens, int32_t num_seqs, int64_t total_tokens,
+                               int32_t H, int32_t d_k, int32_t d_v, kda_dtype_t dtype,
+                               float q_scale, void* o, float* S_final, void* workspace,
+                               size_t workspace_bytes, cudaStream_t stream)
+{
+    if (A == nullptr) return KDA_ERR_INVALID_ARG;
+    const kda::SnapArgs none{0, nullptr, nullptr};
+    const kda::GateArgs gate{A, q_scale};
+    return prefill_impl(q, k, v, z, beta, S0, cu_seqlens, num_seqs, total_tokens, H, d_k, d_v,
+                        dtype, o, S_final, none, gate, workspace, workspace_bytes, stream);
 }
 
 kda_status_t kda_decode_step(const void* q, const void* k, const void* v,
@@ -187,7 +206,28 @@ kda_status_t kda_decode_step(const void* q, const void* k, const void* v,
     if (overlaps(o, (size_t)N * H * d_v * out_bytes(dtype), S_inout, state_bytes))
         return KDA_ERR_INVALID_ARG;
     cudaError_t err = kda::launch_decode(q, k, v, log_alpha, beta, S_inout, N, H, d_k,
-                                         dtype, o, stream);
+                                         dtype, o, kda::GateArgs{nullptr, 1.f}, stream);
+    return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+kda_status_t kda_decode_step_fused(const void* q, const void* k, const void* v, const float* z,
+                                   const float* A, const float* beta, float* S_inout, int32_t N,
+                                   int32_t H, int32_t d_k, int32_t d_v, kda_dtype_t dtype,
+                                   float q_scale, void* o, cudaStream_t stream)
+{
+    if (!valid_dtype(dtype)) return KDA_ERR_UNSUPPORTED;
+    if (d_k != d_v || !supported_d(d_k)) return KDA_ERR_UNSUPPORTED;
+    if (N < 1 || H < 1) return KDA_ERR_INVALID_ARG;
+    if (!q || !k || !v || !z || !A || !beta || !S_inout || !o) return KDA_ERR_INVALID_ARG;
+    const void* ptrs16[] = {q, k, v, z, A, o, S_inout};
+    for (const void* p : ptrs16)
+        if (!aligned(p, 16)) return KDA_ERR_INVALID_ARG;
+    if (!aligned(beta, 4)) return KDA_ERR_INVALID_ARG;
+    const size_t state_bytes = (size_t)N * H * d_k * d_v * sizeof(float);
+    if (overlaps(o, (size_t)N * H * d_v * out_bytes(dtype), S_inout, state_bytes))
+        return KDA_ERR_INVALID_ARG;
+    cudaError_t err = kda::launch_decode(q, k, v, z, beta, S_inout, N, H, d_k, dtype, o,
+                                         kda::GateArgs{A, q_scale}, stream);
     return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
@@ -211,7 +251,7 @@ kda_status_t kda_decode_multi(const void* q, const void* k, const void* v,
         overlaps(o, o_bytes, S_in, state_bytes))
         return KDA_ERR_INVALID_ARG;
     cudaError_t err = kda::launch_decode_multi(q, k, v, log_alpha, beta, S_in, states, N, Ts, H,
-                                               d_k, dtype, o, stream);
+                                               d_k, dtype, o, kda::GateArgs{nullptr, 1.f}, stream);
     return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 

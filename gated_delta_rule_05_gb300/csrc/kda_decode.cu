@@ -21,6 +21,12 @@
 // state once, applies Ts steps to it in registers and writes each step's state
 // to its own slot; the one-token decode is the case Ts = 1 written in place.
 //
+// With the gate prologue (A not null; "[논문 리뷰] Kimi K3 Technical Report",
+// section 3.5) the log_alpha input is the gate pre-activation z,
+// g = -5 sigmoid(e^A z), and q, k are L2-normalised in the kernel: the sums
+// of squares are reduced across the block with k.q, and the norms scale k and
+// q where they are used (a factor of exactly 1 without the prologue).
+//
 // Mapping: one CTA per (sequence, head, value-column slab).  Value columns of
 // S never mix (column j is updated with v_j alone), so a slab is independent.
 // Each thread holds R float4 of its slab in registers between the read and the
@@ -54,7 +60,8 @@ __global__ void __launch_bounds__(THREADS)
 decode_kernel(const TI* __restrict__ q, const TI* __restrict__ k,
               const TI* __restrict__ v, const float* __restrict__ log_alpha,
               const float* __restrict__ beta, const float* S_in, float* S_out,
-              TO* __restrict__ o, int dv, int Ts, int H)
+              TO* __restrict__ o, int dv, int Ts, int H, const float* __restrict__ gateA,
+              float q_scale)
 {
     using Sh = DecodeShape<DK, DVS, THREADS>;
     constexpr int LPR = Sh::kLanesPerRow;
@@ -84,8 +91,10 @@ decode_kernel(const TI* __restrict__ q, const TI* __restrict__ k,
     __shared__ float sh_a[DK], sh_k[DK], sh_ak[DK], sh_aq[DK];
     __shared__ float sh_red_w[Sh::kWarps][DVS];
     __shared__ float sh_red_p[Sh::kWarps][DVS];
-    __shared__ float sh_kq[Sh::kWarps];
+    __shared__ float sh_kq[Sh::kWarps], sh_kk[Sh::kWarps], sh_qq[Sh::kWarps];
     __shared__ float sh_u[DVS];
+    const bool fused = gateA != nullptr;
+    const float eA = (fused && tid < DK) ? expf(gateA[h * DK + tid]) : 0.f;
 
     for (int t = 0; t < Ts; ++t) {
         const long long tok = (n * Ts + t) * H + h;       // token row of this (n, t, h)
@@ -93,10 +102,11 @@ decode_kernel(const TI* __restrict__ q, const TI* __restrict__ k,
         if (t > 0) __syncthreads();                        // the previous token's reads are done
 
         // 2. Token inputs: alpha, k, alpha.*k, alpha.*q and the partial k.q.
-        float kq = 0.f;
+        float kq = 0.f, kk2 = 0.f, qq2 = 0.f;
         if (tid < DK) {
             const long long off = tok * DK + tid;
-            const float a = expf(log_alpha[off]);
+            const float gg = fused ? gate_from_z(log_alpha[off], eA) : log_alpha[off];
+            const float a = expf(gg);
             const float kk = ld_f(k + off);
             const float qq = ld_f(q + off);
             sh_a[tid] = a;
@@ -104,11 +114,35 @@ decode_kernel(const TI* __restrict__ q, const TI* __restrict__ k,
             sh_ak[tid] = a * kk;
             sh_aq[tid] = a * qq;
             kq = kk * qq;
+            kk2 = kk * kk;
+            qq2 = qq * qq;
         }
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, off);
-        if (lane == 0) sh_kq[warp] = kq;
+        for (int off = 16; off > 0; off >>= 1) {
+            kq += __shfl_xor_sync(0xffffffffu, kq, off);
+            if (fused) {
+                kk2 += __shfl_xor_sync(0xffffffffu, kk2, off);
+                qq2 += __shfl_xor_sync(0xffffffffu, qq2, off);
+            }
+        }
+        if (lane == 0) {
+            sh_kq[warp] = kq;
+            sh_kk[warp] = kk2;
+            sh_qq[warp] = qq2;
+        }
         __syncthreads();
+        // 1 / ||k|| and q_scale / ||q|| (exactly 1 without the prologue)
+        float ik = 1.f, iq = 1.f;
+        if (fused) {
+            float sk = 0.f, sq = 0.f;
+#pragma unroll
+            for (int i = 0; i < Sh::kWarps; ++i) {
+                sk += sh_kk[i];
+                sq += sh_qq[i];
+            }
+            ik = inv_norm(sk);
+            iq = q_scale * inv_norm(sq);
+        }
 
         // 3. Partial column sums of S^T(alpha.*k) and S^T(alpha.*q) over this
         //    thread's rows, then across lanes that share the same columns.
@@ -116,7 +150,7 @@ decode_kernel(const TI* __restrict__ q, const TI* __restrict__ k,
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             const int i = rg + r * RPP;
-            const float ak = sh_ak[i], aq = sh_aq[i];
+            const float ak = sh_ak[i] * ik, aq = sh_aq[i] * iq;
             w.x = fmaf(ak, s[r].x, w.x); w.y = fmaf(ak, s[r].y, w.y);
             w.z = fmaf(ak, s[r].z, w.z); w.w = fmaf(ak, s[r].w, w.w);
             p.x = fmaf(aq, s[r].x, p.x); p.y = fmaf(aq, s[r].y, p.y);
@@ -153,7 +187,7 @@ decode_kernel(const TI* __restrict__ q, const TI* __restrict__ k,
             const int j = slab * DVS + tid;
             const long long vo = tok * dv + j;
             const float u = beta[tok] * (ld_f(v + vo) - ws);
-            st_f(o + vo, fmaf(kqs, u, ps));
+            st_f(o + vo, fmaf(kqs * ik * iq, u, ps));
             sh_u[tid] = u;
         }
         __syncthreads();
@@ -164,7 +198,7 @@ decode_kernel(const TI* __restrict__ q, const TI* __restrict__ k,
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             const int i = rg + r * RPP;
-            const float a = sh_a[i], kk = sh_k[i];
+            const float a = sh_a[i], kk = sh_k[i] * ik;
             float4 x;
             x.x = fmaf(a, s[r].x, kk * u4.x);
             x.y = fmaf(a, s[r].y, kk * u4.y);
@@ -198,7 +232,8 @@ state_gather_kernel(const float* __restrict__ states, const float* S_in,
 template <typename TI, typename TO, int D>
 cudaError_t launch_typed(const void* q, const void* k, const void* v,
                          const float* g, const float* beta, const float* S_in, float* S_out,
-                         int32_t N, int32_t Ts, int32_t H, void* o, cudaStream_t stream)
+                         int32_t N, int32_t Ts, int32_t H, void* o, const GateArgs& gate,
+                         cudaStream_t stream)
 {
     // Slab widths and thread counts: 32 KiB of state per CTA at d = 128
     // (8 float4 per thread), one warp-row pattern per smaller head size.
@@ -209,20 +244,21 @@ cudaError_t launch_typed(const void* q, const void* k, const void* v,
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     decode_kernel<TI, TO, D, DVS, THREADS><<<(unsigned)blocks, THREADS, 0, stream>>>(
         static_cast<const TI*>(q), static_cast<const TI*>(k), static_cast<const TI*>(v),
-        g, beta, S_in, S_out, static_cast<TO*>(o), D, Ts, H);
+        g, beta, S_in, S_out, static_cast<TO*>(o), D, Ts, H, gate.A, gate.q_scale);
     return cudaGetLastError();
 }
 
 template <typename TI, typename TO>
 cudaError_t launch_d(int32_t d, const void* q, const void* k, const void* v,
                      const float* g, const float* beta, const float* S_in, float* S_out,
-                     int32_t N, int32_t Ts, int32_t H, void* o, cudaStream_t stream)
+                     int32_t N, int32_t Ts, int32_t H, void* o, const GateArgs& gate,
+                     cudaStream_t stream)
 {
     switch (d) {
-        case 16: return launch_typed<TI, TO, 16>(q, k, v, g, beta, S_in, S_out, N, Ts, H, o, stream);
-        case 32: return launch_typed<TI, TO, 32>(q, k, v, g, beta, S_in, S_out, N, Ts, H, o, stream);
-        case 64: return launch_typed<TI, TO, 64>(q, k, v, g, beta, S_in, S_out, N, Ts, H, o, stream);
-        case 128: return launch_typed<TI, TO, 128>(q, k, v, g, beta, S_in, S_out, N, Ts, H, o, stream);
+        case 16: return launch_typed<TI, TO, 16>(q, k, v, g, beta, S_in, S_out, N, Ts, H, o, gate, stream);
+        case 32: return launch_typed<TI, TO, 32>(q, k, v, g, beta, S_in, S_out, N, Ts, H, o, gate, stream);
+        case 64: return launch_typed<TI, TO, 64>(q, k, v, g, beta, S_in, S_out, N, Ts, H, o, gate, stream);
+        case 128: return launch_typed<TI, TO, 128>(q, k, v, g, beta, S_in, S_out, N, Ts, H, o, gate, stream);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -230,18 +266,18 @@ cudaError_t launch_d(int32_t d, const void* q, const void* k, const void* v,
 cudaError_t launch_multi(const void* q, const void* k, const void* v, const float* log_alpha,
                          const float* beta, const float* S_in, float* S_out, int32_t N,
                          int32_t Ts, int32_t H, int32_t d, kda_dtype_t dtype, void* o,
-                         cudaStream_t stream)
+                         const GateArgs& gate, cudaStream_t stream)
 {
     switch (dtype) {
         case KDA_BF16:
             return launch_d<__nv_bfloat16, __nv_bfloat16>(d, q, k, v, log_alpha, beta, S_in, S_out,
-                                                          N, Ts, H, o, stream);
+                                                          N, Ts, H, o, gate, stream);
         case KDA_BF16_F32OUT:
             return launch_d<__nv_bfloat16, float>(d, q, k, v, log_alpha, beta, S_in, S_out, N, Ts,
-                                                  H, o, stream);
+                                                  H, o, gate, stream);
         default:
             return launch_d<float, float>(d, q, k, v, log_alpha, beta, S_in, S_out, N, Ts, H, o,
-                                          stream);
+                                          gate, stream);
     }
 }
 
@@ -250,17 +286,19 @@ cudaError_t launch_multi(const void* q, const void* k, const void* v, const floa
 cudaError_t launch_decode(const void* q, const void* k, const void* v,
                           const float* log_alpha, const float* beta, float* S,
                           int32_t N, int32_t H, int32_t d, kda_dtype_t dtype,
-                          void* o, cudaStream_t stream)
+                          void* o, const GateArgs& gate, cudaStream_t stream)
 {
-    return launch_multi(q, k, v, log_alpha, beta, S, S, N, 1, H, d, dtype, o, stream);
+    return launch_multi(q, k, v, log_alpha, beta, S, S, N, 1, H, d, dtype, o, gate, stream);
 }
 
 cudaError_t launch_decode_multi(const void* q, const void* k, const void* v,
                                 const float* log_alpha, const float* beta, const float* S_in,
                                 float* states, int32_t N, int32_t Ts, int32_t H, int32_t d,
-                                kda_dtype_t dtype, void* o, cudaStream_t stream)
+                                kda_dtype_t dtype, void* o, const GateArgs& gate,
+                                cudaStream_t stream)
 {
-    return launch_multi(q, k, v, log_alpha, beta, S_in, states, N, Ts, H, d, dtype, o, stream);
+    return launch_multi(q, k, v, log_alpha, beta, S_in, states, N, Ts, H, d, dtype, o, gate,
+                        stream);
 }
 
 cudaError_t launch_state_gather(const float* states, const float* S_in, const int32_t* accept,

@@ -80,6 +80,25 @@ inline bool split_plan(int32_t num_seqs, int32_t H, int sms, SplitPlan* plan) {
 // Number of SMs of the current device (cached per device; 0 on failure).
 int device_sm_count();
 
+// The gate prologue fused into the kernels ("[논문 리뷰] Kimi K3 Technical
+// Report", section 3.5), when A is not null: the log_alpha input then holds
+// the gate pre-activation z, g = -5 sigmoid(e^A z) with A [H, d_k] fp32, and
+// q and k are L2-normalised over the key channels inside the kernel, q also
+// multiplied by q_scale.  A null A: log_alpha is g and q, k are used as given.
+struct GateArgs {
+    const float* A;
+    float q_scale;
+};
+
+__device__ __forceinline__ float gate_from_z(float z, float eA)
+{
+    // -5 sigmoid(e^A z) = -5 / (1 + e^{-e^A z}); the limits -5 and 0 are exact
+    return __fdividef(-5.f, 1.f + __expf(-eA * z));
+}
+
+// 1 / ||x|| of a row whose sum of squares is ss (a zero row stays zero).
+__device__ __forceinline__ float inv_norm(float ss) { return rsqrtf(fmaxf(ss, 1e-30f)); }
+
 // Prefix-state snapshots requested from a prefill (interval 0: none).
 // Snapshot j of sequence n, the state after its first (j + 1) * interval
 // tokens, goes to out + ((offsets[n] + j) * H + h) * d_k * d_v; offsets is
@@ -112,14 +131,15 @@ cudaError_t launch_worklist(const int32_t* cu_seqlens, int32_t num_seqs,
 cudaError_t launch_decode(const void* q, const void* k, const void* v,
                           const float* log_alpha, const float* beta, float* S,
                           int32_t N, int32_t H, int32_t d, kda_dtype_t dtype,
-                          void* o, cudaStream_t stream);
+                          void* o, const GateArgs& gate, cudaStream_t stream);
 
 // Ts tokens per sequence from S_in, the state after each token to `states`
 // ([N, Ts, H, d, d]); the one-token decode above is the case Ts = 1 in place.
 cudaError_t launch_decode_multi(const void* q, const void* k, const void* v,
                                 const float* log_alpha, const float* beta, const float* S_in,
                                 float* states, int32_t N, int32_t Ts, int32_t H, int32_t d,
-                                kda_dtype_t dtype, void* o, cudaStream_t stream);
+                                kda_dtype_t dtype, void* o, const GateArgs& gate,
+                                cudaStream_t stream);
 
 cudaError_t launch_state_gather(const float* states, const float* S_in, const int32_t* accept,
                                 int32_t N, int32_t Ts, int32_t H, int32_t d_k, int32_t d_v,
@@ -131,7 +151,7 @@ cudaError_t launch_prefill_simt(const void* q, const void* k, const void* v,
                                 int32_t num_seqs, int64_t total_tokens, int32_t H,
                                 int32_t d, kda_dtype_t dtype, void* o,
                                 float* S_final, const int32_t* ws, const SnapArgs& snap,
-                                cudaStream_t stream);
+                                const GateArgs& gate, cudaStream_t stream);
 
 // Tensor-core prefill (bf16 q/k/v, d = 128).  Returns false when the call
 // must take the CUDA-core path instead (other dtypes or head sizes, no tokens,
@@ -142,13 +162,14 @@ cudaError_t launch_prefill_tc(const void* q, const void* k, const void* v,
                               const float* log_alpha, const float* beta, const float* S0,
                               const int32_t* cu_seqlens, int32_t num_seqs, int64_t total_tokens,
                               int32_t H, kda_dtype_t dtype, void* o, float* S_final,
-                              int32_t* ws, const SnapArgs& snap, cudaStream_t stream);
+                              int32_t* ws, const SnapArgs& snap, const GateArgs& gate,
+                              cudaStream_t stream);
 
 cudaError_t launch_prefill_split(const void* q, const void* k, const void* v,
                                  const float* log_alpha, const float* beta, const float* S0,
                                  const int32_t* cu_seqlens, int32_t num_seqs,
                                  int64_t total_tokens, int32_t H, kda_dtype_t dtype, void* o,
                                  float* S_final, int32_t* ws, const SplitPlan& plan,
-                                 const SnapArgs& snap, cudaStream_t stream);
+                                 const SnapArgs& snap, const GateArgs& gate, cudaStream_t stream);
 
 }  // namespace kda

@@ -17,6 +17,9 @@
 //     (I + A) U = Diag(beta) (V - (gamma .* K) S0)         (forward substitution)
 //     O         = (gamma .* Q) S0 + P U
 //     S_C       = Diag(gamma_last) S0 + sum_i ((gamma_last / gamma_i) .* k_i) u_i^T
+// With the gate prologue (see GateArgs) phase 0 forms each chunk row's q and k
+// norms and phase 1 turns z into g = -5 sigmoid(e^A z) and scales q and k.
+//
 // The decay is normalised to the chunk start, as the pages require for long
 // chunks.  exp(G_rc - G_ic) is factored as exp(G_rc) * exp(-G_ic); with
 // g >= -5 (the lower bound of section 3.5) and 16 tokens per chunk the larger
@@ -50,7 +53,8 @@ struct SimtSmem {
     static constexpr int kP = kA + kC * (kC + 1);
     static constexpr int kB = kP + kC * (kC + 1);
     static constexpr int kGl = kB + kC;
-    static constexpr int kFloats = kGl + DK;
+    static constexpr int kInv = kGl + DK;    // gate prologue: 1/||q_r|| (x q_scale), 1/||k_r||
+    static constexpr int kFloats = kInv + 2 * kC;
     static constexpr size_t kBytes = kFloats * sizeof(float);
 };
 
@@ -62,7 +66,7 @@ prefill_simt_kernel(const TI* __restrict__ q, const TI* __restrict__ k,
                     const int32_t* __restrict__ cu, const int32_t* __restrict__ ws,
                     long long total_tokens, int H, TO* __restrict__ o,
                     float* S_final,   // may alias S0: no __restrict__ on either
-                    const SnapArgs snap)
+                    const SnapArgs snap, const GateArgs gate)
 {
     using L = SimtSmem<DK, DVS>;
     constexpr int LD = L::LD, LDS = L::LDS;
@@ -81,8 +85,11 @@ prefill_simt_kernel(const TI* __restrict__ q, const TI* __restrict__ k,
     float* sP = sm + L::kP;
     float* sB = sm + L::kB;
     float* sGl = sm + L::kGl;
+    float* sInv = sm + L::kInv;
+    const bool fused = gate.A != nullptr;
 
     const int tid = threadIdx.x;
+    const int lane = tid & 31, warp = tid >> 5;
     const int item = blockIdx.x;
     const int rank = item / (H * NSLAB);
     const int h = (item / NSLAB) % H;
@@ -99,6 +106,8 @@ prefill_simt_kernel(const TI* __restrict__ q, const TI* __restrict__ k,
     }
     const long long sbase = ((long long)n * H + h) * DK * DV;
     const int seq_off = (cu != nullptr && snap.interval > 0) ? snap.offsets[n] : 0;
+    // e^A of this thread's key channel (gate prologue)
+    const float eA = (fused && tid < DK) ? expf(gate.A[h * DK + tid]) : 0.f;
 
     for (int e = tid; e < DK * DVS; e += kThreads) {
         const int c = e / DVS, j = e % DVS;
@@ -107,6 +116,26 @@ prefill_simt_kernel(const TI* __restrict__ q, const TI* __restrict__ k,
 
     for (long long t0 = bos; t0 < eos; t0 += kC) {
         __syncthreads();
+        // Phase 0 (gate prologue only): the inverse norms of the chunk's q
+        // and k rows, one warp per (row, tensor) pair.
+        if (fused) {
+            for (int pr = warp; pr < 2 * kC; pr += kThreads / 32) {
+                const int r = pr >> 1;
+                const long long t = t0 + r;
+                float ss = 0.f;
+                if (t < eos) {
+                    const TI* row = ((pr & 1) ? k : q) + (t * H + h) * DK;
+                    for (int c = lane; c < DK; c += 32) {
+                        const float x = ld_f(row + c);
+                        ss = fmaf(x, x, ss);
+                    }
+                }
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+                if (lane == 0) sInv[pr] = (pr & 1) ? inv_norm(ss) : gate.q_scale * inv_norm(ss);
+            }
+            __syncthreads();
+        }
         // Phase 1: gates, decayed operands; v slab and beta.
         if (tid < DK) {
             const int c = tid;
@@ -121,6 +150,11 @@ prefill_simt_kernel(const TI* __restrict__ q, const TI* __restrict__ k,
                     gg = g[off];
                     kk = ld_f(k + off);
                     qq = ld_f(q + off);
+                    if (fused) {
+                        gg = gate_from_z(gg, eA);
+                        qq *= sInv[2 * r];
+                        kk *= sInv[2 * r + 1];
+                    }
                 }
                 G += gg;
                 const float gam = expf(G);
@@ -226,7 +260,7 @@ cudaError_t launch_typed(const void* q, const void* k, const void* v,
                          const float* g, const float* beta, const float* S0,
                          const int32_t* cu, int32_t N, int64_t T_tot, int32_t H,
                          void* o, float* S_final, const int32_t* ws, const SnapArgs& snap,
-                         cudaStream_t stream)
+                         const GateArgs& gate, cudaStream_t stream)
 {
     constexpr int DVS = D < 32 ? D : 32;
     using L = SimtSmem<D, DVS>;
@@ -243,7 +277,7 @@ cudaError_t launch_typed(const void* q, const void* k, const void* v,
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     kern<<<(unsigned)blocks, kThreads, L::kBytes, stream>>>(
         static_cast<const TI*>(q), static_cast<const TI*>(k), static_cast<const TI*>(v),
-        g, beta, S0, cu, ws, (long long)T_tot, H, static_cast<TO*>(o), S_final, snap);
+        g, beta, S0, cu, ws, (long long)T_tot, H, static_cast<TO*>(o), S_final, snap, gate);
     return cudaGetLastError();
 }
 
@@ -252,13 +286,13 @@ cudaError_t launch_d(int32_t d, const void* q, const void* k, const void* v,
                      const float* g, const float* beta, const float* S0,
                      const int32_t* cu, int32_t N, int64_t T_tot, int32_t H,
                      void* o, float* S_final, const int32_t* ws, const SnapArgs& snap,
-                     cudaStream_t stream)
+                     const GateArgs& gate, cudaStream_t stream)
 {
     switch (d) {
-        case 16: return launch_typed<TI, TO, 16>(q, k, v, g, beta, S0, cu, N, T_tot, H, o, S_final, ws, snap, stream);
-        case 32: return launch_typed<TI, TO, 32>(q, k, v, g, beta, S0, cu, N, T_tot, H, o, S_final, ws, snap, stream);
-        case 64: return launch_typed<TI, TO, 64>(q, k, v, g, beta, S0, cu, N, T_tot, H, o, S_final, ws, snap, stream);
-        case 128: return launch_typed<TI, TO, 128>(q, k, v, g, beta, S0, cu, N, T_tot, H, o, S_final, ws, snap, stream);
+        case 16: return launch_typed<TI, TO, 16>(q, k, v, g, beta, S0, cu, N, T_tot, H, o, S_final, ws, snap, gate, stream);
+        case 32: return launch_typed<TI, TO, 32>(q, k, v, g, beta, S0, cu, N, T_tot, H, o, S_final, ws, snap, gate, stream);
+        case 64: return launch_typed<TI, TO, 64>(q, k, v, g, beta, S0, cu, N, T_tot, H, o, S_final, ws, snap, gate, stream);
+        case 128: return launch_typed<TI, TO, 128>(q, k, v, g, beta, S0, cu, N, T_tot, H, o, S_final, ws, snap, gate, stream);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -271,18 +305,18 @@ cudaError_t launch_prefill_simt(const void* q, const void* k, const void* v,
                                 int32_t num_seqs, int64_t total_tokens, int32_t H,
                                 int32_t d, kda_dtype_t dtype, void* o,
                                 float* S_final, const int32_t* ws, const SnapArgs& snap,
-                                cudaStream_t stream)
+                                const GateArgs& gate, cudaStream_t stream)
 {
     switch (dtype) {
         case KDA_BF16:
             return launch_d<__nv_bfloat16, __nv_bfloat16>(d, q, k, v, log_alpha, beta, S0, cu_seqlens,
-                                                          num_seqs, total_tokens, H, o, S_final, ws, snap, stream);
+                                                          num_seqs, total_tokens, H, o, S_final, ws, snap, gate, stream);
         case KDA_BF16_F32OUT:
             return launch_d<__nv_bfloat16, float>(d, q, k, v, log_alpha, beta, S0, cu_seqlens,
-                                                  num_seqs, total_tokens, H, o, S_final, ws, snap, stream);
+                                                  num_seqs, total_tokens, H, o, S_final, ws, snap, gate, stream);
         default:
             return launch_d<float, float>(d, q, k, v, log_alpha, beta, S0, cu_seqlens, num_seqs,
-                                          total_tokens, H, o, S_final, ws, snap, stream);
+                                          total_tokens, H, o, S_final, ws, snap, gate, stream);
     }
 }
 

@@ -302,11 +302,13 @@ __device__ __forceinline__ void consumer(const Ctx& X, uint32_t tmem, int warp, 
 }
 
 // ------------------------------------------------------------- producer
+template <bool FUSED>
 __device__ __forceinline__ void producer(const Ctx& X, uint32_t tmem, int warp, int lane,
                                          const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                                          const CUtensorMap* tm_g, const float* beta,
                                          const int32_t* cu, int32_t* ws, long long total_tokens,
-                                         int H, int U, int R, int32_t* flags, uint8_t* ring)
+                                         int H, int U, int R, int32_t* flags, uint8_t* ring,
+                                         const GateArgs& gate)
 {
     uint8_t* sm = X.sm;
     JobDesc* jd = reinterpret_cast<JobDesc*>(sm + OFF_JOB);
@@ -375,6 +377,9 @@ __device__ __forceinline__ void producer(const Ctx& X, uint32_t tmem, int warp, 
                 const long long tt = t0 + r;
                 sBin[r] = (tt < eos) ? beta[tt * H + hh] : 0.f;
             }
+            if (FUSED)   // the head's A row, read by gate prep (like beta)
+                reinterpret_cast<float4*>(sm + OFF_AH)[lane] =
+                    reinterpret_cast<const float4*>(gate.A + (long long)hh * kD)[lane];
             __syncwarp();
             if (lane == 0) {
                 JobDesc& j = jd[jc & 1];
@@ -451,7 +456,10 @@ __device__ __forceinline__ void producer(const Ctx& X, uint32_t tmem, int warp, 
             int32_t seen = (ct == 0 && job.c >= R) ? ld_relaxed_gpu(consumed + job.u) : want;
             float2 Gq[16];
             PassParams pp;
-            const int npass = gate_prep(X, t, len, reinterpret_cast<const float*>(sm + P_G), Gq, pp);
+            if (FUSED) qk_norms(X, t, gate.q_scale);
+            const float* sG = reinterpret_cast<const float*>(sm + P_G);
+            const float* Ah = reinterpret_cast<const float*>(sm + OFF_AH);
+            const int npass = gate_prep<FUSED>(X, t, len, sG, Ah, Gq, pp);
             bool alive = true;
             for (int p = 0; p < npass; ++p) {
                 const Pass ps = select_pass(pp, p, npass, len);
@@ -462,7 +470,7 @@ __device__ __forceinline__ void producer(const Ctx& X, uint32_t tmem, int warp, 
                 }
                 group_sync();
                 pass_factors(X, t, ps, reinterpret_cast<float*>(sm + OFF_GL));
-                gram_operands(X, t, ps, Gq, sm + P_QG, sm + P_KT);
+                gram_operands<FUSED>(X, t, ps, Gq, sm + P_QG, sm + P_KT);
                 fence_proxy_async_smem();
                 group_sync();
                 if (ct == 0) {
@@ -515,14 +523,15 @@ __device__ __forceinline__ void producer(const Ctx& X, uint32_t tmem, int warp, 
 }
 
 // ------------------------------------------------------------- the kernel
-template <typename TO>
+// FUSED: the gate prologue runs in the producers (gate.A not null).
+template <typename TO, bool FUSED>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_split_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUtensorMap tm_v,
                      const __grid_constant__ CUtensorMap tm_o, const float* __restrict__ beta,
                      const float* S0, const int32_t* __restrict__ cu, int32_t* ws,
                      long long total_tokens, int H, TO* __restrict__ o, float* S_final, int U, int R,
-                     int32_t* flags, uint8_t* ring, const SnapArgs snap)
+                     int32_t* flags, uint8_t* ring, const SnapArgs snap, const GateArgs gate)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -556,8 +565,8 @@ prefill_split_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         consumer<TO>(X, tmem, warp, lane, &tm_v, &tm_o, S0, cu, ws, total_tokens, H, o, S_final, U,
                      R, flags, ring, snap);
     else
-        producer(X, tmem, warp, lane, &tm_q, &tm_k, &tm_g, beta, cu, ws, total_tokens, H, U, R,
-                 flags, ring);
+        producer<FUSED>(X, tmem, warp, lane, &tm_q, &tm_k, &tm_g, beta, cu, ws, total_tokens, H, U,
+                        R, flags, ring, gate);
 
     tc_fence_before();
     __syncthreads();
@@ -567,11 +576,11 @@ prefill_split_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     }
 }
 
-template <typename TO>
+template <typename TO, bool FUSED>
 cudaError_t launch_typed(const void* q, const void* k, const void* v, const float* g,
                          const float* beta, const float* S0, const int32_t* cu, int64_t T,
                          int32_t H, void* o, float* S_final, int32_t* ws, const SplitPlan& plan,
-                         const SnapArgs& snap, cudaStream_t stream)
+                         const SnapArgs& snap, const GateArgs& gate, cudaStream_t stream)
 {
     CUtensorMap mq, mk, mg, mv, mo;
     const bool bf16_out = sizeof(TO) == 2;
@@ -583,7 +592,7 @@ cudaError_t launch_typed(const void* q, const void* k, const void* v, const floa
         !tc_make_map(&mv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, T, 64, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     if (!bf16_out) mo = mq;
-    auto kern = prefill_split_kernel<TO>;
+    auto kern = prefill_split_kernel<TO, FUSED>;
     static bool attr_set = false;   // benign race: every writer stores the same value
     if (!attr_set) {
         const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -611,7 +620,7 @@ cudaError_t launch_typed(const void* q, const void* k, const void* v, const floa
     cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, kern, mq, mk, mg, mv, mo, beta, S0, cu, ws, (long long)T, (int)H,
                            static_cast<TO*>(o), S_final, (int)plan.units, (int)plan.ring, flags,
-                           ring, snap);
+                           ring, snap, gate);
     if (e != cudaSuccess && debug_enabled())
         fprintf(stderr, "kda: prefill_split launch failed: %s\n", cudaGetErrorString(e));
     return e;
@@ -624,14 +633,23 @@ cudaError_t launch_prefill_split(const void* q, const void* k, const void* v,
                                  const int32_t* cu_seqlens, int32_t num_seqs,
                                  int64_t total_tokens, int32_t H, kda_dtype_t dtype, void* o,
                                  float* S_final, int32_t* ws, const SplitPlan& plan,
-                                 const SnapArgs& snap, cudaStream_t stream)
+                                 const SnapArgs& snap, const GateArgs& gate, cudaStream_t stream)
 {
     (void)num_seqs;
+    const bool fused = gate.A != nullptr;
     if (dtype == KDA_BF16_F32OUT)
-        return launch_typed<float>(q, k, v, log_alpha, beta, S0, cu_seqlens, total_tokens, H, o,
-                                   S_final, ws, plan, snap, stream);
-    return launch_typed<__nv_bfloat16>(q, k, v, log_alpha, beta, S0, cu_seqlens, total_tokens, H,
-                                       o, S_final, ws, plan, snap, stream);
+        return fused ? launch_typed<float, true>(q, k, v, log_alpha, beta, S0, cu_seqlens,
+                                                 total_tokens, H, o, S_final, ws, plan, snap, gate,
+                                                 stream)
+                     : launch_typed<float, false>(q, k, v, log_alpha, beta, S0, cu_seqlens,
+                                                  total_tokens, H, o, S_final, ws, plan, snap, gate,
+                                                  stream);
+    return fused ? launch_typed<__nv_bfloat16, true>(q, k, v, log_alpha, beta, S0, cu_seqlens,
+                                                     total_tokens, H, o, S_final, ws, plan, snap,
+                                                     gate, stream)
+                 : launch_typed<__nv_bfloat16, false>(q, k, v, log_alpha, beta, S0, cu_seqlens,
+                                                      total_tokens, H, o, S_final, ws, plan, snap,
+                                                      gate, stream);
 }
 
 }  // namespace kda

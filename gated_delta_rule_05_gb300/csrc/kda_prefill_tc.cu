@@ -83,14 +83,16 @@ using namespace tc;
 constexpr int kThreads = 320;
 
 // ------------------------------------------------------------- the kernel
-template <typename TO>
+// FUSED: the gate prologue runs in the kernel (gate.A not null).
+template <typename TO, bool FUSED>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUtensorMap tm_v,
                   const __grid_constant__ CUtensorMap tm_o,
                   const float* __restrict__ beta, const float* S0,
                   const int32_t* __restrict__ cu, int32_t* ws, long long total_tokens, int H,
-                  TO* __restrict__ o, float* S_final, const SnapArgs snap)
+                  TO* __restrict__ o, float* S_final, const SnapArgs snap,
+                  const GateArgs gate)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -206,6 +208,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         const Lane t = make_lane(tid - 64, warp, lane);
         const int ct = t.ct;
         const int seq_off = (cu != nullptr && snap.interval > 0) ? snap.offsets[n] : 0;
+        const float* Ah = FUSED ? gate.A + (long long)h * kD : nullptr;
         state_load(t, tmem, S0, sbase);
 
         int step = 0, chunk_v = 0;
@@ -216,7 +219,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             if (!group_wait(X, B_QKG_FULL, ch)) break;
             float2 Gq[16];
             PassParams pp;
-            const int npass = gate_prep(X, t, len, reinterpret_cast<const float*>(sm + OFF_G), Gq, pp);
+            if (FUSED) qk_norms(X, t, gate.q_scale);
+            const float* sG = reinterpret_cast<const float*>(sm + OFF_G);
+            const int npass = gate_prep<FUSED>(X, t, len, sG, Ah, Gq, pp);
             for (int p = 0; p < npass; ++p) {
                 const Pass ps = select_pass(pp, p, npass, len);
                 pass_factors(X, t, ps, reinterpret_cast<float*>(sm + OFF_GL));
@@ -237,7 +242,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 // stats before the lo parts overwrite the g tile.
                 if (ct == 0) bulk_wait_group_read0();
                 group_sync();
-                gram_operands(X, t, ps, Gq, sm + OFF_QG, sm + OFF_KT);
+                gram_operands<FUSED>(X, t, ps, Gq, sm + OFF_QG, sm + OFF_KT);
                 fence_proxy_async_smem();
                 group_sync();
                 if (ct == 0) mbar_arrive(&X.bar[B_OPS]);
@@ -301,11 +306,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
 }
 
-template <typename TO>
+template <typename TO, bool FUSED>
 cudaError_t launch_typed(const void* q, const void* k, const void* v, const float* g,
                          const float* beta, const float* S0, const int32_t* cu, int32_t N,
                          int64_t T, int32_t H, void* o, float* S_final, int32_t* ws,
-                         const SnapArgs& snap, cudaStream_t stream)
+                         const SnapArgs& snap, const GateArgs& gate, cudaStream_t stream)
 {
     CUtensorMap mq, mk, mg, mv, mo;
     // The output map is used for bf16 output only (fp32 output is stored by
@@ -318,7 +323,7 @@ cudaError_t launch_typed(const void* q, const void* k, const void* v, const floa
         !tc_make_map(&mg, g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, H, T, kD, CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !tc_make_map(&mv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, T, 64, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
-    auto kern = prefill_tc_kernel<TO>;
+    auto kern = prefill_tc_kernel<TO, FUSED>;
     static bool attr_set = false;   // benign race: every writer stores the same value
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -336,7 +341,8 @@ cudaError_t launch_typed(const void* q, const void* k, const void* v, const floa
     if (!bf16_out) mo = mq;
     kern<<<(unsigned)blocks, kThreads, kSmemBytes, stream>>>(mq, mk, mg, mv, mo, beta, S0, cu, ws,
                                                             (long long)T, H,
-                                                            static_cast<TO*>(o), S_final, snap);
+                                                            static_cast<TO*>(o), S_final, snap,
+                                                            gate);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess && debug_enabled())
         fprintf(stderr, "kda: prefill_tc launch failed: %s\n", cudaGetErrorString(e));
@@ -356,13 +362,22 @@ cudaError_t launch_prefill_tc(const void* q, const void* k, const void* v,
                               const float* log_alpha, const float* beta, const float* S0,
                               const int32_t* cu_seqlens, int32_t num_seqs, int64_t total_tokens,
                               int32_t H, kda_dtype_t dtype, void* o, float* S_final,
-                              int32_t* ws, const SnapArgs& snap, cudaStream_t stream)
+                              int32_t* ws, const SnapArgs& snap, const GateArgs& gate,
+                              cudaStream_t stream)
 {
+    const bool fused = gate.A != nullptr;
     if (dtype == KDA_BF16_F32OUT)
-        return launch_typed<float>(q, k, v, log_alpha, beta, S0, cu_seqlens, num_seqs,
-                                   total_tokens, H, o, S_final, ws, snap, stream);
-    return launch_typed<__nv_bfloat16>(q, k, v, log_alpha, beta, S0, cu_seqlens, num_seqs,
-                                       total_tokens, H, o, S_final, ws, snap, stream);
+        return fused ? launch_typed<float, true>(q, k, v, log_alpha, beta, S0, cu_seqlens, num_seqs,
+                                                 total_tokens, H, o, S_final, ws, snap, gate, stream)
+                     : launch_typed<float, false>(q, k, v, log_alpha, beta, S0, cu_seqlens,
+                                                  num_seqs, total_tokens, H, o, S_final, ws, snap,
+                                                  gate, stream);
+    return fused ? launch_typed<__nv_bfloat16, true>(q, k, v, log_alpha, beta, S0, cu_seqlens,
+                                                     num_seqs, total_tokens, H, o, S_final, ws, snap,
+                                                     gate, stream)
+                 : launch_typed<__nv_bfloat16, false>(q, k, v, log_alpha, beta, S0, cu_seqlens,
+                                                      num_seqs, total_tokens, H, o, S_final, ws,
+                                                      snap, gate, stream);
 }
 
 }  // namespace kda

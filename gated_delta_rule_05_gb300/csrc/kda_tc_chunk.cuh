@@ -83,7 +83,9 @@ constexpr uint32_t OFF_A32 = 196608;   // A, then X = (I+A)^-1: fp32 [64][68]; b
 constexpr uint32_t OFF_BDLO = OFF_A32; //   Gram readout: Gram B lo part [ch][Kc lo] bf16
 constexpr uint32_t OFF_T16 = 214016;   // T       [r][i] fp16 (V product); during gate prep:
 constexpr uint32_t OFF_STAT = OFF_T16; //   per row-quarter decay stats, fp32 [3][4][128]
-constexpr uint32_t OFF_Y = 222208;     // 3 KB not used by the phases
+constexpr uint32_t OFF_Y = 222208;     // 3 KB: the first 1 KB not used by the phases, then
+constexpr uint32_t OFF_NRM = OFF_Y + 1024;    // gate prologue: q_scale/||q_r|| [64], 1/||k_r|| [64]
+constexpr uint32_t OFF_AH = OFF_Y + 1536;     // gate prologue: the head's A row [128] (split producer)
 // Solve tiles, in regions idle during the solve (the g tile's and the Gram
 // B tile's space; the next q/k/g load waits for the first three):
 constexpr uint32_t OFF_DF = OFF_G;            // D blocks, fp32 [4][16][17] (padded rows)
@@ -278,22 +280,68 @@ struct Pass {
 };
 
 // ---------------------------------------------------------------------------
+// Front phase 0 (gate prologue only): the inverse L2 norms of the chunk's q
+// and k rows, from the bf16 tiles in shared memory, to OFF_NRM.  Thread ct
+// sums 32 channels of row ct / 4 (16-byte loads rotated by the row, so that a
+// warp's loads hit distinct banks); four threads combine.  Ends with a group
+// barrier.
+__device__ __forceinline__ void qk_norms(const Ctx& X, const Lane& t, float q_scale)
+{
+    const int r = t.ct >> 2, qq = t.ct & 3;
+    float sq = 0.f, sk = 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int jj = (j + r) & 3;
+        const uint32_t off = r * 256 + 64 * qq + 16 * jj;
+        const uint4 a = *reinterpret_cast<const uint4*>(X.sm + OFF_Q + off);
+        const uint4 b = *reinterpret_cast<const uint4*>(X.sm + OFF_K + off);
+        const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float q0 = lo_bf16(av[e]), q1 = hi_bf16(av[e]);
+            const float k0 = lo_bf16(bv[e]), k1 = hi_bf16(bv[e]);
+            sq = fmaf(q0, q0, fmaf(q1, q1, sq));
+            sk = fmaf(k0, k0, fmaf(k1, k1, sk));
+        }
+    }
+#pragma unroll
+    for (int off = 1; off < 4; off <<= 1) {
+        sq += __shfl_xor_sync(0xffffffffu, sq, off);
+        sk += __shfl_xor_sync(0xffffffffu, sk, off);
+    }
+    float* nrm = reinterpret_cast<float*>(X.sm + OFF_NRM);
+    if (qq == 0) {
+        nrm[r] = q_scale * inv_norm(sq);
+        nrm[64 + r] = inv_norm(sk);
+    }
+    group_sync();
+}
+
+// ---------------------------------------------------------------------------
 // Front phase 1: decay scan of this thread's 16 rows x 2 channels of the g
 // tile sG ([64][128] fp32; log2 units, relative to the start of its row
 // quarter, kept in Gq), the two-pass vote and both pass layouts' factors.
-// Returns the number of passes (1, 2).
+// With the gate prologue (FUSED) the tile holds z and g = -5 sigmoid(e^A z),
+// Ah = the head's A row (d_k values).  Returns the number of passes (1, 2).
+template <bool FUSED>
 __device__ __forceinline__ int gate_prep(const Ctx& X, const Lane& t, int len, const float* sG,
-                                         float2 (&Gq)[16], PassParams& pp)
+                                         const float* Ah, float2 (&Gq)[16], PassParams& pp)
 {
     const int cp = t.cp, rq = t.rq;
+    const float2 eA = FUSED ? make_float2(expf(Ah[2 * cp]), expf(Ah[2 * cp + 1]))
+                            : make_float2(0.f, 0.f);
     float* sStat = reinterpret_cast<float*>(X.sm + OFF_STAT);   // [3][4][128]
     {
         float2 G = make_float2(0.f, 0.f), mx = G, mn = G;
 #pragma unroll
         for (int rr = 0; rr < 16; ++rr) {
             const int r = 16 * rq + rr;
-            const float2 g = (r < len) ? *reinterpret_cast<const float2*>(sG + r * kD + 2 * cp)
-                                       : make_float2(0.f, 0.f);
+            float2 g = (r < len) ? *reinterpret_cast<const float2*>(sG + r * kD + 2 * cp)
+                                 : make_float2(0.f, 0.f);
+            if (FUSED && r < len) {
+                g.x = gate_from_z(g.x, eA.x);
+                g.y = gate_from_z(g.y, eA.y);
+            }
             G.x = fmaf(g.x, kLog2e, G.x);
             G.y = fmaf(g.y, kLog2e, G.y);
             Gq[rr] = G;
@@ -396,11 +444,14 @@ __device__ __forceinline__ void pass_factors(const Ctx& X, const Lane& t, const 
 
 // Front phase 3: the Gram operands (bf16 hi/lo) in shared memory, and
 // (e^G Q)^T and Ktil^T (fp16) to qg_dst / kt_dst; this thread writes
-// 2 channels x 2 chunks of 8 rows of each.  No barrier.
+// 2 channels x 2 chunks of 8 rows of each.  With the gate prologue (FUSED)
+// q and k are scaled by their rows' inverse norms (OFF_NRM).  No barrier.
+template <bool FUSED>
 __device__ __forceinline__ void gram_operands(const Ctx& X, const Lane& t, const Pass& ps,
                                               const float2 (&Gq)[16], uint8_t* qg_dst,
                                               uint8_t* kt_dst)
 {
+    const float* nrm = reinterpret_cast<const float*>(X.sm + OFF_NRM);
     const int cp = t.cp, rq = t.rq, lo = ps.lo, hi = ps.hi;
     const uint8_t* sQ = X.sm + OFF_Q;
     const uint8_t* sK = X.sm + OFF_K;
@@ -425,8 +476,12 @@ __device__ __forceinline__ void gram_operands(const Ctx& X, const Lane& t, const
                 for (int w = 0; w < 2; ++w) {
                     const int w8 = 2 * e + w, rr = 8 * jj + w8, r = 16 * rq + rr;
                     const bool act = (r >= lo && r < hi);
-                    const float kk = u ? hi_bf16(kp[w8]) : lo_bf16(kp[w8]);
-                    const float qq = u ? hi_bf16(qp[w8]) : lo_bf16(qp[w8]);
+                    float kk = u ? hi_bf16(kp[w8]) : lo_bf16(kp[w8]);
+                    float qq = u ? hi_bf16(qp[w8]) : lo_bf16(qp[w8]);
+                    if (FUSED) {
+                        kk *= nrm[64 + r];
+                        qq *= nrm[r];
+                    }
                     const float gv = u ? Gq[rr].y : Gq[rr].x;
                     const float x = ps.basec[u] + gv - ps.Rc[u];
                     const float e1 = act ? ex2(x) : 0.f;

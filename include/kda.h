@@ -159,6 +159,34 @@ kda_status_t kda_prefill_snapshots(const void *q, const void *k, const void *v,
                                    float *snapshots, void *workspace,
                                    size_t workspace_bytes, cudaStream_t stream);
 
+/* kda_prefill with the steps in front of the recurrence fused into the
+ * kernels ("Kimi 모델 분석", section "커널 최적화": one kernel for the KDA
+ * layer): the lower-bounded decay of "[논문 리뷰] Kimi K3 Technical Report",
+ * section 3.5,
+ *     g = -5 Sigmoid(e^A z),   alpha = exp(g) in (e^-5, 1),
+ * and the L2 normalisation of q and k over the key channels (q then
+ * multiplied by q_scale, typically d_k^-1/2).
+ *
+ * Arguments and results are those of kda_prefill, except:
+ *   q, k   raw (not normalised) in the input dtype; each row of d_k values
+ *          must be nonzero
+ *   z      [T_tot, H, d_k] fp32, the gate pre-activation (in place of
+ *          log_alpha)
+ *   A      [H, d_k] fp32, 16-byte aligned (a per-head A is its value repeated
+ *          over the channels); NULL is KDA_ERR_INVALID_ARG
+ *   q_scale  the factor applied to the normalised q
+ * Normalised q and k enter the products in fp32 before any rounding to the
+ * operand precision, so the result is at least as accurate as calling
+ * kda_prefill on q, k normalised and rounded by the caller. */
+kda_status_t kda_prefill_fused(const void *q, const void *k, const void *v,
+                               const float *z, const float *A, const float *beta,
+                               const float *S0, const int32_t *cu_seqlens,
+                               int32_t num_seqs, int64_t total_tokens, int32_t H,
+                               int32_t d_k, int32_t d_v, kda_dtype_t dtype,
+                               float q_scale, void *o, float *S_final,
+                               void *workspace, size_t workspace_bytes,
+                               cudaStream_t stream);
+
 /* One decode step for N independent sequences (one new token each): the
  * recurrence above applied once per (sequence, head), state updated in place.
  * Decode reads and writes a fixed 2 * 4 * d_k * d_v bytes of fp32 state per
@@ -176,6 +204,16 @@ kda_status_t kda_decode_step(const void *q, const void *k, const void *v,
                              float *S_inout, int32_t N, int32_t H, int32_t d_k,
                              int32_t d_v, kda_dtype_t dtype, void *o,
                              cudaStream_t stream);
+
+/* kda_decode_step with the gate prologue fused (see kda_prefill_fused): z
+ * [N, H, d_k] fp32 in place of log_alpha, A [H, d_k] fp32, raw q and k
+ * (nonzero rows), q_scale. */
+kda_status_t kda_decode_step_fused(const void *q, const void *k, const void *v,
+                                   const float *z, const float *A,
+                                   const float *beta, float *S_inout, int32_t N,
+                                   int32_t H, int32_t d_k, int32_t d_v,
+                                   kda_dtype_t dtype, float q_scale, void *o,
+                                   cudaStream_t stream);
 
 /* Several decode tokens per sequence, keeping the state after every token:
  * the verification step of speculative decoding, which must be able to
