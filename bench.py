@@ -554,10 +554,16 @@ def host_memory_available():
     return avail if avail is not None else 8 << 30
 
 
+E2E_SEGMENT_TOKENS = 16384
+
+
 def run_e2e(kda, torch, inp, dev, stream, args, world):
-    """Same metric through the public API with host buffers: every step copies
-    the step's inputs from pinned host memory, runs kda_prefill and reads o
-    back to pinned host memory."""
+    """Same metric through the C ABI with HOST buffers: kda_prefill_host takes
+    the step's inputs in pinned host memory and returns o to pinned host
+    memory, pipelining copies in, compute and copies out over segments of
+    E2E_SEGMENT_TOKENS tokens on three streams.  Every copy is inside the
+    timed region: the copy-in stream waits for the start event, and the
+    compute stream (which the end event follows) waits for the last copy out."""
     T_full, H, d = inp.q.shape
     # Pinned host memory is capped at 30 % of what the host reports available;
     # if the whole batch does not fit, the e2e leg runs on its first T tokens
@@ -565,33 +571,29 @@ def run_e2e(kda, torch, inp, dev, stream, args, world):
     per_token = H * BYTES_PER_TOKEN_HEAD
     budget = int(0.3 * host_memory_available())
     T = min(T_full, max(64, budget // per_token // 64 * 64))
+    # The host buffers are written by the CPU first, as a caller's prompt
+    # buffers are: pinned pages that only the GPU has touched are mapped for
+    # it lazily and the first passes over them run at a fraction of the link
+    # rate (measured: 37, then 66, then 193 GB/s for 17 GB device-to-host).
     host = {}
     try:
         for name in ("q", "k", "v", "log_alpha", "beta"):
             t = getattr(inp, name)[:T]
             h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+            h.zero_()
             h.copy_(t)
             host[name] = h
-        cu = torch.tensor([0, T], dtype=torch.int32)
-        host["cu_seqlens"] = cu.pin_memory()
         o_host = torch.empty((T, H, d), dtype=inp.q.dtype, pin_memory=True)
+        o_host.zero_()
     except RuntimeError as exc:
         return {"value": None, "unit": "tokens/s", "error": "pinned allocation failed: %s" % exc}
     torch.cuda.synchronize(dev)
-    dbuf = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
-    o_dev = torch.empty((T, H, d), dtype=inp.q.dtype, device=dev)
-    ws = torch.empty(kda.kda_prefill_workspace_bytes(1, H, d, d), dtype=torch.uint8, device=dev)
-    kernel = prefill_kernel_name(ws.numel(), 1)
+    hp = kda.HostPrefill(H, d, inp.q.dtype, segment_tokens=E2E_SEGMENT_TOKENS, device=dev)
     h2d = sum(v.numel() * v.element_size() for v in host.values())
     d2h = o_host.numel() * o_host.element_size()
 
     def step():
-        for k, v in host.items():
-            dbuf[k].copy_(v, non_blocking=True)
-        kda.kda_prefill(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["log_alpha"], dbuf["beta"],
-                        cu_seqlens=dbuf["cu_seqlens"], o=o_dev, want_state=False,
-                        workspace=ws, stream=stream)
-        o_host.copy_(o_dev, non_blocking=True)
+        hp(host["q"], host["k"], host["v"], host["log_alpha"], host["beta"], o_host)
 
     steps = max(1, min(args.steps, 5))
     for _ in range(min(args.warmup, 2)):
@@ -599,19 +601,42 @@ def run_e2e(kda, torch, inp, dev, stream, args, world):
     torch.cuda.synchronize(dev)
     barrier(world)
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s.record(stream)
+    s.record(hp.compute)
+    hp.h2d.wait_event(s)
     for _ in range(steps):
         step()
-    e.record(stream)
+    e.record(hp.compute)
     torch.cuda.synchronize(dev)
     barrier(world)
     ms = max_over_ranks(s.elapsed_time(e), world, dev)
     res = {"value": T * world * steps / (ms / 1e3), "unit": "tokens/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
            "ms_per_step": ms / steps, "tokens_per_step_per_gpu": T,
-           "whole_batch": T == T_full}
-    del host, dbuf, o_host, o_dev
+           "whole_batch": T == T_full, "api": "kda_prefill_host",
+           "segment_tokens": E2E_SEGMENT_TOKENS,
+           "link_gbs": host_link_rates(torch, dev, hp.h2d)}
+    del host, o_host, hp
     return res
+
+
+def host_link_rates(torch, dev, stream, nbytes=1 << 29, reps=8):
+    """Plain pinned-copy rates of the host link right after the e2e leg (the
+    e2e leg is bound by them and they vary between hosts and over time)."""
+    h = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    h.zero_()
+    g = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    out = {}
+    for name, dst, src in (("h2d", g, h), ("d2h", h, g)):
+        with torch.cuda.stream(stream):
+            dst.copy_(src, non_blocking=True)          # first pass maps the pages
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record(stream)
+            for _ in range(reps):
+                dst.copy_(src, non_blocking=True)
+            e.record(stream)
+        torch.cuda.synchronize(dev)
+        out[name] = nbytes * reps / (s.elapsed_time(e) / 1e3) / 1e9
+    return out
 
 
 def main(argv=None):

@@ -11,6 +11,7 @@ Functions (same names as the C ABI):
   kda_decode_step(q, k, v, log_alpha, beta, S_inout, ...)
   kda_decode_multi(q, k, v, log_alpha, beta, S_in, ...)
   kda_prefill_fused(q, k, v, z, A, beta, ..., q_scale)
+  kda_prefill_host(q, k, v, log_alpha, beta (host), ..., segment_tokens)
   kda_decode_step_fused(q, k, v, z, A, beta, S_inout, ..., q_scale)
   kda_state_gather(states, S_in, accept, ...)
   kda_prefill_workspace_bytes(num_seqs, H, d_k, d_v)
@@ -31,7 +32,7 @@ KDA_BF16, KDA_FP32, KDA_BF16_F32OUT = 0, 1, 2
 EXPORTS = ("kda_prefill_workspace_bytes", "kda_prefill", "kda_decode_step",
            "kda_status_string", "kda_prefill_noalloc", "kda_prefill_snapshots",
            "kda_decode_multi", "kda_state_gather", "kda_prefill_fused",
-           "kda_decode_step_fused")
+           "kda_decode_step_fused", "kda_prefill_host_staging_bytes", "kda_prefill_host")
 
 
 class KdaError(RuntimeError):
@@ -61,6 +62,11 @@ def _declare(lib):
                                     _i32, _i32, _i32, _i32, ctypes.c_int, _vp, _vp]
     lib.kda_status_string.restype = ctypes.c_char_p
     lib.kda_status_string.argtypes = [ctypes.c_int]
+    lib.kda_prefill_host_staging_bytes.restype = _sz
+    lib.kda_prefill_host_staging_bytes.argtypes = [_i32, _i32, _i32, ctypes.c_int, _i64]
+    lib.kda_prefill_host.restype = ctypes.c_int
+    lib.kda_prefill_host.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i32, _i32, _i32,
+                                     ctypes.c_int, _vp, _vp, _vp, _sz, _i64, _vp, _vp, _vp]
     lib.kda_prefill_fused.restype = ctypes.c_int
     lib.kda_prefill_fused.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                       _i32, _i64, _i32, _i32, _i32, ctypes.c_int, ctypes.c_float,
@@ -446,3 +452,44 @@ def kda_decode_step_fused(q, k, v, z, A, beta, S_inout, *, q_scale, o=None, stre
     if rc != KDA_OK:
         raise KdaError(rc, "kda_decode_step_fused")
     return o
+
+
+class HostPrefill:
+    """kda_prefill_host for repeated calls: holds the device staging area and
+    the three streams the pipeline runs on (C ABI: kda_prefill_host).
+
+        hp = HostPrefill(H, d, dtype=torch.bfloat16, segment_tokens=16384)
+        hp(q_h, k_h, v_h, log_alpha_h, beta_h, o_h, S0=None, S_final=None)
+
+    q_h, k_h, v_h, log_alpha_h, beta_h, o_h are CPU tensors (pinned for full
+    speed) of one sequence; S0 / S_final are CUDA tensors [1, H, d, d] or
+    None.  The call returns once the work is enqueued; hp.compute (a torch
+    stream) completes when everything has, o_h included."""
+
+    def __init__(self, H, d, dtype, segment_tokens=16384, o_dtype=None, device=None):
+        torch = _torch()
+        self.H, self.d, self.seg = H, d, int(segment_tokens)
+        self.device = torch.device("cuda", torch.cuda.current_device()) if device is None \
+            else torch.device(device)
+        probe = torch.empty(0, dtype=dtype)
+        self.dt = _dtype_code(probe, o_dtype or dtype)
+        nbytes = int(lib().kda_prefill_host_staging_bytes(H, d, d, self.dt, self.seg))
+        if nbytes == 0:
+            raise KdaError(KDA_ERR_INVALID_ARG, "kda_prefill_host_staging_bytes")
+        self.staging = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
+        self.compute = torch.cuda.Stream(self.device)
+        self.h2d = torch.cuda.Stream(self.device)
+        self.d2h = torch.cuda.Stream(self.device)
+
+    def __call__(self, q, k, v, log_alpha, beta, o, S0=None, S_final=None):
+        T = q.shape[0]
+        hp = lambda t: None if t is None else ctypes.c_void_p(t.data_ptr())
+        with _torch().cuda.device(self.device):
+            rc = lib().kda_prefill_host(
+                hp(q), hp(k), hp(v), hp(log_alpha), hp(beta), _ptr(S0), T, self.H, self.d,
+                self.d, self.dt, hp(o), _ptr(S_final), _ptr(self.staging),
+                self.staging.numel(), self.seg, ctypes.c_void_p(self.compute.cuda_stream),
+                ctypes.c_void_p(self.h2d.cuda_stream), ctypes.c_void_p(self.d2h.cuda_stream))
+        if rc != KDA_OK:
+            raise KdaError(rc, "kda_prefill_host")
+        return o, S_final

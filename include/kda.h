@@ -12,9 +12,10 @@
  *     alpha_t = exp(log_alpha_t)       (per key channel), beta_t a scalar.
  *
  * Conventions shared by every call:
- *  - All pointers are DEVICE pointers unless stated otherwise; the caller
- *    owns every buffer.  The library allocates nothing and keeps no state
- *    between calls other than cached device attributes.
+ *  - All pointers are DEVICE pointers unless stated otherwise (only
+ *    kda_prefill_host takes host buffers); the caller owns every buffer.  The
+ *    library allocates nothing and keeps no state between calls other than
+ *    cached device attributes.
  *  - Work is enqueued on `stream`; no call synchronises the host.  Argument
  *    errors are returned synchronously before anything is launched; a launch
  *    failure returns KDA_ERR_CUDA.  Nothing is thrown across the ABI.
@@ -186,6 +187,49 @@ kda_status_t kda_prefill_fused(const void *q, const void *k, const void *v,
                                float q_scale, void *o, float *S_final,
                                void *workspace, size_t workspace_bytes,
                                cudaStream_t stream);
+
+/* Device staging bytes kda_prefill_host needs for segments of
+ * segment_tokens tokens (a multiple of 64): two input and two output segment
+ * buffers, two state buffers and a prefill workspace.  0 for bad arguments. */
+size_t kda_prefill_host_staging_bytes(int32_t H, int32_t d_k, int32_t d_v,
+                                      kda_dtype_t dtype, int64_t segment_tokens);
+
+/* kda_prefill of ONE sequence whose token inputs and output live in HOST
+ * memory (a long prompt that arrives from the host).  The sequence is cut into
+ * segments of segment_tokens tokens (a positive multiple of 64) that flow
+ * through a pipeline: copies in on `h2d`, kda_prefill on `compute` (the state
+ * carried from segment to segment, "Kimi 모델 분석", section "순환을 GPU에
+ * 올리기": only the state passes between chunks), copies out on `d2h`, so that
+ * the three overlap.  The result equals kda_prefill over the whole sequence
+ * bit for bit.
+ *
+ *   q, k, v, log_alpha, beta, o   HOST pointers, layouts of kda_prefill with
+ *                 N = 1 (page-locked memory for full copy bandwidth; pageable
+ *                 memory works, with slower copies).  Page-locked pages that
+ *                 the CPU has never written are mapped for the GPU on first
+ *                 access, and the first passes over them copy at a fraction of
+ *                 the link rate; buffers the host filled run at full rate.
+ *   S0, S_final   DEVICE [H, d_k, d_v] fp32 or NULL, as in kda_prefill
+ *   staging       DEVICE buffer of kda_prefill_host_staging_bytes(...) bytes,
+ *                 256-byte aligned, not shared with concurrent calls
+ *   compute, h2d, d2h  three streams (distinct for overlap).  When `compute`
+ *                 is complete, so is everything the call enqueued.  The first
+ *                 copy in waits for the work already on `compute` (a previous
+ *                 call on the same staging area, the producer of S0).
+ * The pipeline fills and drains over one segment, so shorter segments bound
+ * the overhead; 16384 tokens keep each segment's launches well above their
+ * fixed cost.
+ * The call creates six CUDA events and releases them before it returns; it
+ * allocates no memory and does not synchronise the host.  Argument errors are
+ * returned before anything is enqueued. */
+kda_status_t kda_prefill_host(const void *q, const void *k, const void *v,
+                              const float *log_alpha, const float *beta,
+                              const float *S0, int64_t total_tokens, int32_t H,
+                              int32_t d_k, int32_t d_v, kda_dtype_t dtype,
+                              void *o, float *S_final, void *staging,
+                              size_t staging_bytes, int64_t segment_tokens,
+                              cudaStream_t compute, cudaStream_t h2d,
+                              cudaStream_t d2h);
 
 /* One decode step for N independent sequences (one new token each): the
  * recurrence above applied once per (sequence, head), state updated in place.
