@@ -77,20 +77,13 @@ struct JobDesc {
 };
 constexpr uint32_t OFF_JOB = OFF_Y;        // 2 JobDesc (unused by the front phases)
 static_assert(OFF_JOB + 2 * sizeof(JobDesc) <= OFF_GL, "job area overflows");
-// Producer-only uses of space that only the single-CTA kernel's back phases
-// need.  The g tile lives apart from the Gram lo parts and solve tiles (which
-// reuse OFF_G), so that the next job's q / k / g load can start as soon as
-// pass B is done.  The operand tiles are staged in shared memory and sent to
-// the ring with bulk copies (e^{G_last} from OFF_GL): written straight from
-// registers, each warp store of the swizzled tiles would touch 32 different
-// lines.
-constexpr uint32_t P_G = OFF_WT;          // g tile [64][128] fp32
-constexpr uint32_t P_QG = OFF_V;          // (e^G Q)^T staging, then -W^T staging, 16 KB
-constexpr uint32_t P_KT = OFF_KT;         // Ktil^T staging, 16 KB
-constexpr uint32_t P_P = OFF_P;           // P staging, 8 KB
-constexpr uint32_t P_T16 = OFF_T16;       // T staging, 8 KB (the decay stats' space)
-static_assert(P_G + 32768 <= P_P && P_P + 8192 <= P_KT && P_KT + 16384 <= OFF_A32,
-              "producer staging overlaps");
+// The producer's operand tiles are staged in the front map's tiles (-W^T,
+// (e^G Q)^T, P, Ktil^T, T) and sent to the ring with bulk copies (e^{G_last}
+// from OFF_GL): written straight from registers, each warp store of the
+// swizzled tiles would touch 32 different lines.  The (e^G K)^T tile takes
+// the v tile's place (a producer has no v), so the q / k / g tiles are free
+// for the next job's load as soon as pass B is done.
+constexpr uint32_t P_GK = OFF_V;
 
 constexpr long long kPollTimeout = 1ll << 32;   // ~2 s of SM clock
 
@@ -393,7 +386,7 @@ __device__ __forceinline__ void producer(const Ctx& X, uint32_t tmem, int warp, 
                 mbar_arrive_expect_tx(&X.bar[B_QKG_FULL], 2 * 16384 + 32768);
                 tma_load_2d(sm + OFF_Q, tm_q, hh * kD, (int32_t)t0, &X.bar[B_QKG_FULL]);
                 tma_load_2d(sm + OFF_K, tm_k, hh * kD, (int32_t)t0, &X.bar[B_QKG_FULL]);
-                tma_load_2d(sm + P_G, tm_g, hh * kD, (int32_t)t0, &X.bar[B_QKG_FULL]);
+                tma_load_2d(sm + OFF_G, tm_g, hh * kD, (int32_t)t0, &X.bar[B_QKG_FULL]);
                 ++issued;
                 if (jc > 0) ok = publish(jc - 1);
             }
@@ -411,7 +404,7 @@ __device__ __forceinline__ void producer(const Ctx& X, uint32_t tmem, int warp, 
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA
         // The whole warp runs this loop; the issue helpers elect one lane.
-        const FrontDescs D = make_front_descs(sm);
+        const FrontDescs D = make_front_descs(sm, P_GK);
         for (int step = 0;; ++step) {
             if (!warp_wait(X, B_OPS, step)) break;
             tc_fence_after();
@@ -457,7 +450,7 @@ __device__ __forceinline__ void producer(const Ctx& X, uint32_t tmem, int warp, 
             float2 Gq[16];
             PassParams pp;
             if (FUSED) qk_norms(X, t, gate.q_scale);
-            const float* sG = reinterpret_cast<const float*>(sm + P_G);
+            const float* sG = reinterpret_cast<const float*>(sm + OFF_G);
             const float* Ah = reinterpret_cast<const float*>(sm + OFF_AH);
             const int npass = gate_prep<FUSED>(X, t, len, sG, Ah, Gq, pp);
             bool alive = true;
@@ -470,7 +463,7 @@ __device__ __forceinline__ void producer(const Ctx& X, uint32_t tmem, int warp, 
                 }
                 group_sync();
                 pass_factors(X, t, ps, reinterpret_cast<float*>(sm + OFF_GL));
-                gram_operands<FUSED>(X, t, ps, Gq, sm + P_QG, sm + P_KT);
+                gram_operands<FUSED>(X, t, ps, Gq, sm + OFF_QG, sm + OFF_KT, sm + P_GK);
                 fence_proxy_async_smem();
                 group_sync();
                 if (ct == 0) {
@@ -488,30 +481,27 @@ __device__ __forceinline__ void producer(const Ctx& X, uint32_t tmem, int warp, 
                     // slot holds no further claim that a consumer may need.)
                     if (p == npass - 1) mbar_arrive(&X.bar[B_QKG_EMPTY]);
                     if (free_slot) {
-                        bulk_store(blk + BLK_QG, sm + P_QG, 16384);
-                        bulk_store(blk + BLK_KT, sm + P_KT, 16384);
+                        bulk_store(blk + BLK_QG, sm + OFF_QG, 16384);
+                        bulk_store(blk + BLK_KT, sm + OFF_KT, 16384);
                         bulk_store(blk + BLK_GL, sm + OFF_GL, 512);
                         bulk_commit_group();
                     } else {
                         atomicExch(&X.misc->abort, 1);   // the group stops at its next wait
                     }
                 }
-                if (!gram_readout(X, t, tmem, ps.lo, ps.hi, step, sm + P_P)) { alive = false; break; }
+                if (!gram_readout(X, t, tmem, ps.lo, ps.hi, step, sm + OFF_P)) { alive = false; break; }
                 if (ct == 0) {
-                    bulk_store(blk + BLK_P, sm + P_P, 8192);
+                    bulk_store(blk + BLK_P, sm + OFF_P, 8192);
                     bulk_commit_group();
                 }
-                if (!ut_solve(X, t, tmem, warp, step, false, sm + P_T16)) { alive = false; break; }
+                ut_solve(X, t, sm + OFF_T16);
                 if (ct == 0) {
-                    bulk_store(blk + BLK_T16, sm + P_T16, 8192);
+                    bulk_store(blk + BLK_T16, sm + OFF_T16, 8192);
                     bulk_commit_group();
-                    // -W^T reuses the (e^G Q)^T staging area: its copy (the
-                    // oldest of the three groups in flight) has read it.
-                    bulk_wait_group_read2();
                 }
-                if (!w_readout(X, t, tmem, step, sm + P_QG)) { alive = false; break; }
+                if (!w_readout(X, t, tmem, step, sm + OFF_WT)) { alive = false; break; }
                 if (ct == 0) {
-                    bulk_store(blk + BLK_WT, sm + P_QG, 16384);
+                    bulk_store(blk + BLK_WT, sm + OFF_WT, 16384);
                     bulk_commit_group();
                 }
                 ++step;

@@ -184,7 +184,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         // ------------------------------------------------------------ MMA
         // The whole warp runs this loop; the issue helpers elect one lane.
         if (nch > 0) {
-            const FrontDescs D = make_front_descs(sm);
+            const FrontDescs D = make_front_descs(sm, OFF_G);
             for (int step = 0;; ++step) {
                 if (!warp_wait(X, B_OPS, step)) break;
                 tc_fence_after();
@@ -237,12 +237,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     d.chunk = ch;
                     X.desc[step & 1] = d;
                 }
-                // The previous chunk's O store has read its staging area (the
-                // Gram B lo part goes there), and everyone has read the decay
-                // stats before the lo parts overwrite the g tile.
+                // The previous chunk's O store has read its staging area and
+                // everyone has read the decay stats: both lie in the Gram
+                // operand region.  The (e^G K)^T tile takes the g tile's place.
                 if (ct == 0) bulk_wait_group_read0();
                 group_sync();
-                gram_operands<FUSED>(X, t, ps, Gq, sm + OFF_QG, sm + OFF_KT);
+                gram_operands<FUSED>(X, t, ps, Gq, sm + OFF_QG, sm + OFF_KT, sm + OFF_G);
                 fence_proxy_async_smem();
                 group_sync();
                 if (ct == 0) mbar_arrive(&X.bar[B_OPS]);
@@ -262,9 +262,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 tc_fence_before();
 
                 if (!gram_readout(X, t, tmem, ps.lo, ps.hi, step, sm + OFF_P)) { alive = false; break; }
-                if (!ut_solve(X, t, tmem, warp, step, d.last_pass, sm + OFF_T16)) { alive = false; break; }
+                ut_solve(X, t, sm + OFF_T16);
                 if (!w_readout(X, t, tmem, step, sm + OFF_WT)) { alive = false; break; }
-                if (ct == 0) mbar_arrive(&X.bar[B_CV]);
+                if (ct == 0) {
+                    // The W product has read the (e^G K)^T tile: after the
+                    // chunk's last pass the next q / k / g may load.
+                    if (d.last_pass) mbar_arrive(&X.bar[B_QKG_EMPTY]);
+                    mbar_arrive(&X.bar[B_CV]);
+                }
 
                 // ---- U^T -> fp16 A operand
                 if (!group_wait(X, B_MMA_C, step)) { alive = false; break; }

@@ -151,13 +151,6 @@ __device__ __forceinline__ void bulk_wait_group_read0()
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
-// Waits until at most two of this thread's committed bulk groups have not
-// yet read their source.
-__device__ __forceinline__ void bulk_wait_group_read2()
-{
-    asm volatile("cp.async.bulk.wait_group.read 2;" ::: "memory");
-}
-
 // Waits until every committed bulk store of this thread has completed.
 __device__ __forceinline__ void bulk_wait_group0()
 {
@@ -356,6 +349,12 @@ __host__ __device__ constexpr uint32_t make_idesc_f16(uint32_t M, uint32_t N, bo
            ((b_mn_major ? 1u : 0u) << 16) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
+// Same for kind::tf32 (fp32 containers read as tf32), both operands K-major.
+__host__ __device__ constexpr uint32_t make_idesc_tf32(uint32_t M, uint32_t N)
+{
+    return (1u << 4) | (2u << 7) | (2u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
 // The MMA issue helpers below are executed by all 32 threads of a converged
 // warp: elect.sync picks one lane, which issues the instruction.  Keeping the
 // whole warp on the issuing path lets the compiler hold the descriptors in
@@ -385,6 +384,19 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
         "setp.ne.b32 p, %4, 0;\n\t"
         "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
         "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// D (TMEM) = / += A x B, tf32 operands in shared memory (K = 8 per instruction).
+__device__ __forceinline__ void mma_ss_tf32(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 

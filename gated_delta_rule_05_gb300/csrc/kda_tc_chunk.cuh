@@ -30,22 +30,21 @@
 // masked passes of 32 rows (two steps).  Entries above the diagonal may
 // overflow; they are discarded by selection.
 //
-// Operand precision.  The Gram operands carry the exponent factors and need
-// bf16's range: each is a bf16 hi/lo pair and the Gram sums hi.hi, lo.hi and
-// hi.lo, bringing the factor rounding to about 2^-16.  T, P, U, S, V, W, e^G Q
-// and Ktil are O(1) and enter the tensor cores as fp16 (3 more mantissa bits
-// than bf16).  Accumulation and the state carry are fp32.  |v| and the state
+// Operand precision.  The Gram operands carry the exponent factors and need an
+// 8-bit exponent: they are fp32 values multiplied as tf32 (10-bit mantissa,
+// fp32 accumulation).  T, P, U, S, V, W, e^G Q, e^G K and Ktil are O(1) and
+// enter the tensor cores as fp16 (3 more mantissa bits than bf16).  The UT
+// solve runs in fp32 and the state is carried in fp32.  |v| and the state
 // entries are assumed to stay inside the fp16 range (|x| < 65504).
 //
-// UT solve.  With D the inverse of the 16 x 16 diagonal blocks of L = I + A
-// and N = D A_off (A_off = the blocks below the diagonal), N is nilpotent of
-// order 4, so
-//     (I + A)^{-1} = (I + N)^{-1} D = (I + N^2)(I - N) D,
-// and T = (I + N^2) Z with Z = (I - N) D', D' = D Diag(b).  D (forward
-// substitution) and N (six 16 x 16 block products) are formed on CUDA cores;
-// N^2 and Z are one round of tensor-core products, T = (I + N^2) Z a second
-// (fp16 operands, in tensor memory and shared memory idle at that point of
-// the chunk).
+// UT solve.  X = (I + A)^{-1} by block forward substitution on 16 x 16 blocks,
+// in fp32 on the CUDA cores: the diagonal blocks' inverses X_bb by column-wise
+// substitution, then X_ij = -X_ii sum_{j <= k < i} A_ik X_kj for i > j, in six
+// barrier-separated rounds of 16 x 16 block products that start every product
+// as soon as its factors exist (a lookahead order of the block recurrence).
+// T = X Diag(b).  W = T (e^G K) is then one tensor-core product with the fp16
+// T and (e^G K)^T tiles.
+
 #pragma once
 
 #include <cuda.h>
@@ -69,41 +68,39 @@ constexpr float kSpanMax = 250.f;
 // ---- shared memory map of the front phases (bytes from a 1024-aligned base)
 constexpr uint32_t OFF_Q = 0;          // q tile  [64 tok][128 ch] bf16, plain rows
 constexpr uint32_t OFF_K = 16384;      // k tile  [64][128] bf16
-constexpr uint32_t OFF_G = 32768;      // g tile  [64][128] fp32; after the decay scan:
-constexpr uint32_t OFF_ADLO = OFF_G;   //   Gram A lo parts [ch][Kr lo | Qr lo] bf16
-constexpr uint32_t OFF_V = 65536;      // v tile  2 x [64 tok][64 v], 128B swizzle (bf16 -> fp16)
-constexpr uint32_t OFF_AD = 81920;     // Gram A hi parts [ch][Kr | Qr] bf16, 2 x 16 KB
-constexpr uint32_t OFF_BD = 114688;    // Gram B hi part  [ch][Kc] bf16
-constexpr uint32_t OFF_T = 131072;     // T       [r][i] bf16 (W product)
-constexpr uint32_t OFF_WT = 139264;    // -W^T    [ch][r] fp16
-constexpr uint32_t OFF_QG = 155648;    // (e^G Q)^T [ch][r] fp16
-constexpr uint32_t OFF_P = 172032;     // P       [r][i] fp16
-constexpr uint32_t OFF_KT = 180224;    // Ktil^T  [ch][i] fp16
-constexpr uint32_t OFF_A32 = 196608;   // A, then X = (I+A)^-1: fp32 [64][68]; before the
-constexpr uint32_t OFF_BDLO = OFF_A32; //   Gram readout: Gram B lo part [ch][Kc lo] bf16
-constexpr uint32_t OFF_T16 = 214016;   // T       [r][i] fp16 (V product); during gate prep:
-constexpr uint32_t OFF_STAT = OFF_T16; //   per row-quarter decay stats, fp32 [3][4][128]
-constexpr uint32_t OFF_Y = 222208;     // 3 KB: the first 1 KB not used by the phases, then
+constexpr uint32_t OFF_G = 32768;      // g tile  [64][128] fp32 (after gate prep, in the
+                                       //   single-CTA kernel: the (e^G K)^T tile, 16 KB)
+constexpr uint32_t OFF_V = 65536;      // v tile  2 x [64 tok][64 v], 128B swizzle (bf16 -> fp16);
+                                       //   split producer: the (e^G K)^T tile
+constexpr uint32_t OFF_A = 81920;      // Gram A operand [Kr; Qr] tf32, K-major [128][128] (64 KB)
+constexpr uint32_t OFF_KC = 147456;    // Gram B operand Kc tf32, K-major [64][128] (32 KB)
+// After the Gram product, in the operand region [OFF_A, OFF_QG):
+constexpr uint32_t OFF_A32 = OFF_A;           // A fp32 [64][LDA]
+constexpr uint32_t OFF_X = OFF_A + 17408;     // X = (I + A)^-1 fp32 [64][LDA]
+constexpr uint32_t OFF_ZS = OFF_X + 17408;    // solve scratch, 3 x [16][16] fp32
+constexpr uint32_t OFF_STAT = OFF_ZS + 3072;  // gate prep: decay stats fp32 [3][4][128]
+constexpr uint32_t OFF_T16 = 126976;   // T       [r][i] fp16 (W and V products)
+constexpr uint32_t OFF_WT = 163840;    // -W^T    [ch][r] fp16 (directly before (e^G Q)^T)
+constexpr uint32_t OFF_QG = 180224;    // (e^G Q)^T [ch][r] fp16
+constexpr uint32_t OFF_P = 196608;     // P       [r][i] fp16 (directly before Ktil^T)
+constexpr uint32_t OFF_KT = 204800;    // Ktil^T  [ch][i] fp16
+constexpr uint32_t OFF_OST = OFF_A32;  // O tile staging of the single-CTA kernel
+constexpr uint32_t OFF_Y = 221184;     // 2 KB: the first 1 KB not used by the phases, then
 constexpr uint32_t OFF_NRM = OFF_Y + 1024;    // gate prologue: q_scale/||q_r|| [64], 1/||k_r|| [64]
 constexpr uint32_t OFF_AH = OFF_Y + 1536;     // gate prologue: the head's A row [128] (split producer)
-// Solve tiles, in regions idle during the solve (the g tile's and the Gram
-// B tile's space; the next q/k/g load waits for the first three):
-constexpr uint32_t OFF_DF = OFF_G;            // D blocks, fp32 [4][16][17] (padded rows)
-constexpr uint32_t OFF_IMN = OFF_G + 8192;    // I - N as K-major fp16 A [r][k]
-constexpr uint32_t OFF_NB = OFF_G + 16384;    // N  as MN-major fp16 B [m][c] = K-major A [r][k]
-constexpr uint32_t OFF_DPK = OFF_G + 24576;   // D' as K-major fp16 B [c][m] (column c of D')
-constexpr uint32_t OFF_ZB = OFF_BD;           // Z  as MN-major fp16 B [m][c]
-constexpr uint32_t OFF_OST = OFF_A32;  // O tile staging of the single-CTA kernel
-constexpr uint32_t OFF_GL = 225280;    // e^{G_last} per channel
-constexpr uint32_t OFF_R = 225792;     // 2^R per channel
-constexpr uint32_t OFF_BIN = 226304;   // beta of the loaded chunk
-constexpr uint32_t OFF_BST = 226560;   // beta of the current pass (masked)
-constexpr uint32_t OFF_DESC = 226816;  // 2 step descriptors
-constexpr uint32_t OFF_BAR = 226880;   // mbarriers (kNumBars x 8 B)
-constexpr uint32_t OFF_MISC = 227152;  // tmem base, flags
-constexpr uint32_t kSmemUsed = 227168;
+constexpr uint32_t OFF_GL = 223232;    // e^{G_last} per channel
+constexpr uint32_t OFF_BIN = 223744;   // beta of the loaded chunk
+constexpr uint32_t OFF_BST = 224000;   // beta of the current pass (masked)
+constexpr uint32_t OFF_DESC = 224256;  // 2 step descriptors
+constexpr uint32_t OFF_BAR = 224320;   // mbarriers (kNumBars x 8 B)
+constexpr uint32_t OFF_MISC = 224544;  // tmem base, flags
+constexpr uint32_t kSmemUsed = 224560;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;   // + alignment slack
 constexpr int LDA = 68;                // row stride (floats) of A / X: 16-byte aligned rows
+static_assert(OFF_STAT + 6144 <= OFF_T16 && OFF_T16 + 8192 <= OFF_WT, "post-Gram tiles overlap");
+static_assert(OFF_KC + 32768 == OFF_QG && OFF_A + 65536 == OFF_KC, "operand region");
+static_assert(OFF_QG - OFF_WT == 16384 && OFF_KT - OFF_P == 8192,
+              "the back products read -W^T | (e^G Q)^T and P | Ktil^T as one tile each");
 
 // Byte offsets of the back-phase operands inside one step's block (the same
 // block layout is used in shared memory and in the split kernel's ring):
@@ -119,7 +116,6 @@ constexpr uint32_t kBlkBytes = 66048;
 enum Bar {
     B_QKG_FULL = 0, B_QKG_EMPTY, B_V_FULL, B_V_EMPTY, B_OPS, B_MMA_G, B_T, B_MMA_W,
     B_CV, B_MMA_C, B_U, B_MMA_OS,
-    B_S1, B_R1, B_S2, B_R2,                            // UT solve rounds
     B_JOB_DONE,                                        // split producer: operands written
     B_SV_FULL0, B_SV_FULL1, B_SV_FULL2, B_SV_FULL3,    // split consumer: v tile buffers
     B_SV_EMPTY0, B_SV_EMPTY1, B_SV_EMPTY2, B_SV_EMPTY3,
@@ -130,19 +126,14 @@ static_assert(OFF_BAR + kNumBars * 8 <= OFF_MISC, "barrier area overflows");
 
 // TMEM columns (512 allocated).  C|O and O|S are adjacent so that one MMA
 // can write both of a pair.
-constexpr uint32_t TM_G = 0;      // Gram [Kr rows; Qr rows] x [Kc hi | Kc lo]   128 cols
-constexpr uint32_t TM_W = 0;      // W^T (unscaled) [ch][r], after the solve      64 cols
+constexpr uint32_t TM_G = 0;      // Gram [Kr rows; Qr rows] x Kc                 64 cols
+constexpr uint32_t TM_W = 0;      // W^T [ch][r], after the Gram readout          64 cols
 constexpr uint32_t TM_SB = 128;   // S^T fp16 A operand                           64 cols
 constexpr uint32_t TM_C = 192;    // U^T fp32 [v][r]                              64 cols
 constexpr uint32_t TM_O = 256;    // O^T fp32 [v][r]                              64 cols
 constexpr uint32_t TM_S = 320;    // S^T fp32 [v][ch]                            128 cols
 constexpr uint32_t TM_UB = 448;   // U^T fp16 A operand                           32 cols
 constexpr uint32_t kTmemCols = 512;
-// During the UT solve (rows 0..63 used), in columns otherwise idle then:
-constexpr uint32_t TM_Z = 0;      // Z = (I - N) D', fp32                         64 cols
-constexpr uint32_t TM_N2 = 64;    // N^2, fp32                                    64 cols
-constexpr uint32_t TM_T = TM_C;   // T = (I + N^2) Z, fp32                        64 cols
-constexpr uint32_t TM_IPN = TM_UB;  // I + N^2 as fp16 A operand                  32 cols
 
 struct StepDesc {
     int32_t t0, len, lo, hi, first_pass, last_pass, last_step, chunk;
@@ -216,34 +207,6 @@ __device__ __forceinline__ bool warp_wait(const Ctx& X, int b, uint32_t phase)
 {
     const bool ok = wait_bar(X, b, phase);
     return __all_sync(0xffffffffu, ok) != 0;
-}
-
-// 16 x 16 unit-lower diagonal block inverse, column j (j < 16) of block b by
-// forward substitution; x[r] for r < j is 0 and x[j] is 1.
-__device__ __forceinline__ void diag_block_column(const float* sA, int b, int j, float (&x)[16])
-{
-    const float* L = sA + (b * 16) * LDA + b * 16;
-#pragma unroll
-    for (int r = 0; r < 16; ++r) {
-        float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-        for (int i = 0; i < r; ++i) {
-            if (i & 1) a1 = fmaf(L[r * LDA + i], x[i], a1);
-            else a0 = fmaf(L[r * LDA + i], x[i], a0);
-        }
-        x[r] = (r == j) ? 1.f : ((r < j) ? 0.f : -(a0 + a1));
-    }
-}
-
-// Reads 32 fp32 columns of a TMEM row, converts them to 16 packed fp16 pairs.
-__device__ __forceinline__ void tmem_row_f16(uint32_t taddr, uint32_t (&out)[16])
-{
-    uint32_t d[32];
-    tmem_ld32(taddr, d);
-    tmem_ld_wait();
-#pragma unroll
-    for (int i = 0; i < 16; ++i)
-        out[i] = pack_f16x2(__uint_as_float(d[2 * i]), __uint_as_float(d[2 * i + 1]));
 }
 
 // Per-thread coordinates inside the compute group (ct = 0..255 in the group).
@@ -424,38 +387,51 @@ __device__ __forceinline__ Pass select_pass(const PassParams& pp, int p, int npa
     return s;
 }
 
-// Front phase 2: this pass's per-channel factors (e^{G_last} to gl_dst, 2^R)
-// and the masked beta.  No barrier.
+// Front phase 2: this pass's per-channel e^{G_last} (to gl_dst) and the
+// masked beta.  No barrier.
 __device__ __forceinline__ void pass_factors(const Ctx& X, const Lane& t, const Pass& ps,
                                              float* gl_dst)
 {
     const float* sBin = reinterpret_cast<const float*>(X.sm + OFF_BIN);
     float* sBst = reinterpret_cast<float*>(X.sm + OFF_BST);
-    float* sR = reinterpret_cast<float*>(X.sm + OFF_R);
     if (t.rq == 0) {
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            gl_dst[2 * t.cp + u] = ps.glc[u];
-            sR[2 * t.cp + u] = ps.pRc[u];
-        }
+        for (int u = 0; u < 2; ++u) gl_dst[2 * t.cp + u] = ps.glc[u];
     }
     if (t.ct < kC) sBst[t.ct] = (t.ct >= ps.lo && t.ct < ps.hi) ? sBin[t.ct] : 0.f;
 }
 
-// Front phase 3: the Gram operands (bf16 hi/lo) in shared memory, and
-// (e^G Q)^T and Ktil^T (fp16) to qg_dst / kt_dst; this thread writes
-// 2 channels x 2 chunks of 8 rows of each.  With the gate prologue (FUSED)
-// q and k are scaled by their rows' inverse norms (OFF_NRM).  No barrier.
+// Byte offset of element (row, channel ch) in a K-major tf32 tile with the
+// 128-byte swizzle: 32 channels per 128-byte row, 8-row groups 1024 bytes
+// apart, channel groups of 32 `kstride` bytes apart.
+__device__ __forceinline__ uint32_t tf32_kmajor(int row, int ch, uint32_t kstride)
+{
+    return (uint32_t)(ch >> 5) * kstride + (uint32_t)(row >> 3) * 1024 + (uint32_t)(row & 7) * 128 +
+           ((((uint32_t)(ch & 31) >> 2) ^ (uint32_t)(row & 7)) << 4) + (uint32_t)(ch & 3) * 4;
+}
+
+// Front phase 3: the operands of the Gram product, Kr = k e^{G-R} and
+// Qr = q e^{G-R} (rows 0..63 and 64..127 of the A tile) and Kc = k e^{R-G}
+// (the B tile), fp32 in the K-major tf32 layout; and the fp16 [channel][token]
+// tiles (e^G Q)^T, Ktil^T = (k e^{G_last-G})^T and (e^G K)^T to qg_dst, kt_dst
+// and gk_dst.  This thread: channels 2cp, 2cp+1 of rows 16rq .. 16rq+15.  Each
+// tf32 row store covers both channels (8 bytes; a warp's 32 stores fill two
+// 128-byte rows); the fp16 chunks of the two channels are stored in an order
+// that alternates between lane groups, so that a warp's 16-byte stores spread
+// over all eight swizzle positions.  With the gate prologue (FUSED) q and k
+// are scaled by their rows' inverse norms (OFF_NRM).  No barrier.
 template <bool FUSED>
 __device__ __forceinline__ void gram_operands(const Ctx& X, const Lane& t, const Pass& ps,
                                               const float2 (&Gq)[16], uint8_t* qg_dst,
-                                              uint8_t* kt_dst)
+                                              uint8_t* kt_dst, uint8_t* gk_dst)
 {
     const float* nrm = reinterpret_cast<const float*>(X.sm + OFF_NRM);
     const int cp = t.cp, rq = t.rq, lo = ps.lo, hi = ps.hi;
     const uint8_t* sQ = X.sm + OFF_Q;
     const uint8_t* sK = X.sm + OFF_K;
-    uint8_t* sm = X.sm;
+    uint8_t* sA = X.sm + OFF_A;
+    uint8_t* sKc = X.sm + OFF_KC;
+    const bool swap = ((cp >> 2) & 1) != 0;
 #pragma unroll
     for (int jj = 0; jj < 2; ++jj) {
         uint32_t kp[8], qp[8];             // bf16 pairs (channels 2cp, 2cp+1)
@@ -465,17 +441,16 @@ __device__ __forceinline__ void gram_operands(const Ctx& X, const Lane& t, const
             kp[w8] = *reinterpret_cast<const uint32_t*>(sK + r * 256 + 4 * cp);
             qp[w8] = *reinterpret_cast<const uint32_t*>(sQ + r * 256 + 4 * cp);
         }
-        const int chunk = 2 * rq + jj;
+        uint32_t gq[2][4], kt[2][4], gk[2][4];
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            uint32_t krh[4], krl[4], qrh[4], qrl[4], kch[4], kcl[4], gq[4], kt[4];
+        for (int e = 0; e < 4; ++e) {
+            float vk[2][2], vq[2][2], vc[2][2];      // [channel u][row w]
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                float vk[2], vq[2], vc[2];
+            for (int w = 0; w < 2; ++w) {
+                const int w8 = 2 * e + w, rr = 8 * jj + w8, r = 16 * rq + rr;
+                const bool act = (r >= lo && r < hi);
 #pragma unroll
-                for (int w = 0; w < 2; ++w) {
-                    const int w8 = 2 * e + w, rr = 8 * jj + w8, r = 16 * rq + rr;
-                    const bool act = (r >= lo && r < hi);
+                for (int u = 0; u < 2; ++u) {
                     float kk = u ? hi_bf16(kp[w8]) : lo_bf16(kp[w8]);
                     float qq = u ? hi_bf16(qp[w8]) : lo_bf16(qp[w8]);
                     if (FUSED) {
@@ -486,28 +461,35 @@ __device__ __forceinline__ void gram_operands(const Ctx& X, const Lane& t, const
                     const float x = ps.basec[u] + gv - ps.Rc[u];
                     const float e1 = act ? ex2(x) : 0.f;
                     const float e2 = act ? ex2(-x) : 0.f;
-                    vk[w] = kk * e1;
-                    vq[w] = qq * e1;
-                    vc[w] = kk * e2;
+                    vk[u][w] = kk * e1;
+                    vq[u][w] = qq * e1;
+                    vc[u][w] = kk * e2;
                 }
-                krh[e] = pack_bf16x2(vk[0], vk[1]);
-                qrh[e] = pack_bf16x2(vq[0], vq[1]);
-                kch[e] = pack_bf16x2(vc[0], vc[1]);
-                krl[e] = pack_bf16x2(vk[0] - lo_bf16(krh[e]), vk[1] - hi_bf16(krh[e]));
-                qrl[e] = pack_bf16x2(vq[0] - lo_bf16(qrh[e]), vq[1] - hi_bf16(qrh[e]));
-                kcl[e] = pack_bf16x2(vc[0] - lo_bf16(kch[e]), vc[1] - hi_bf16(kch[e]));
-                gq[e] = pack_f16x2(vq[0] * ps.pRc[u], vq[1] * ps.pRc[u]);
-                kt[e] = pack_f16x2(vc[0] * ps.pLc[u], vc[1] * ps.pLc[u]);
+                *reinterpret_cast<float2*>(sA + tf32_kmajor(r, 2 * cp, 16384)) =
+                    make_float2(vk[0][w], vk[1][w]);
+                *reinterpret_cast<float2*>(sA + tf32_kmajor(64 + r, 2 * cp, 16384)) =
+                    make_float2(vq[0][w], vq[1][w]);
+                *reinterpret_cast<float2*>(sKc + tf32_kmajor(r, 2 * cp, 8192)) =
+                    make_float2(vc[0][w], vc[1][w]);
             }
-            const int c = 2 * cp + u;
-            st_chunk(sm + OFF_AD, c, chunk, make_uint4(krh[0], krh[1], krh[2], krh[3]));
-            st_chunk(sm + OFF_AD + 16384, c, chunk, make_uint4(qrh[0], qrh[1], qrh[2], qrh[3]));
-            st_chunk(sm + OFF_ADLO, c, chunk, make_uint4(krl[0], krl[1], krl[2], krl[3]));
-            st_chunk(sm + OFF_ADLO + 16384, c, chunk, make_uint4(qrl[0], qrl[1], qrl[2], qrl[3]));
-            st_chunk(sm + OFF_BD, c, chunk, make_uint4(kch[0], kch[1], kch[2], kch[3]));
-            st_chunk(sm + OFF_BDLO, c, chunk, make_uint4(kcl[0], kcl[1], kcl[2], kcl[3]));
-            st_chunk(qg_dst, c, chunk, make_uint4(gq[0], gq[1], gq[2], gq[3]));
-            st_chunk(kt_dst, c, chunk, make_uint4(kt[0], kt[1], kt[2], kt[3]));
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                gq[u][e] = pack_f16x2(vq[u][0] * ps.pRc[u], vq[u][1] * ps.pRc[u]);
+                kt[u][e] = pack_f16x2(vc[u][0] * ps.pLc[u], vc[u][1] * ps.pLc[u]);
+                gk[u][e] = pack_f16x2(vk[u][0] * ps.pRc[u], vk[u][1] * ps.pRc[u]);
+            }
+        }
+        const int chunk = 2 * rq + jj;
+#pragma unroll
+        for (int o = 0; o < 2; ++o) {
+            const bool u1 = (o == 1) != swap;
+            const int c = 2 * cp + (u1 ? 1 : 0);
+            st_chunk(qg_dst, c, chunk, u1 ? make_uint4(gq[1][0], gq[1][1], gq[1][2], gq[1][3])
+                                          : make_uint4(gq[0][0], gq[0][1], gq[0][2], gq[0][3]));
+            st_chunk(kt_dst, c, chunk, u1 ? make_uint4(kt[1][0], kt[1][1], kt[1][2], kt[1][3])
+                                          : make_uint4(kt[0][0], kt[0][1], kt[0][2], kt[0][3]));
+            st_chunk(gk_dst, c, chunk, u1 ? make_uint4(gk[1][0], gk[1][1], gk[1][2], gk[1][3])
+                                          : make_uint4(gk[0][0], gk[0][1], gk[0][2], gk[0][3]));
         }
     }
 }
@@ -524,13 +506,9 @@ __device__ __forceinline__ bool gram_readout(const Ctx& X, const Lane& t, uint32
     float* sA = reinterpret_cast<float*>(X.sm + OFF_A32);
     const int L = t.L, half = t.half;
     {
-        uint32_t dg[32], dl[32];
+        uint32_t dg[32];
         tmem_ld32(tmem + t.lane_base + TM_G + 32 * half, dg);
-        tmem_ld32(tmem + t.lane_base + TM_G + 64 + 32 * half, dl);
         tmem_ld_wait();
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-            dg[i] = __float_as_uint(__uint_as_float(dg[i]) + __uint_as_float(dl[i]));
         if (L < kC) {
             const int r = L;
             const bool act_r = (r >= lo && r < hi);
@@ -574,189 +552,165 @@ __device__ __forceinline__ bool gram_readout(const Ctx& X, const Lane& t, uint32
     return true;
 }
 
-// Front phase 5: the UT solve (CUDA-core part; the MMA warp runs the two
-// product rounds, mma_front below).  Leaves T as bf16 in shared memory (the
-// W product) and as fp16 at t16_dst.  Arrives B_QKG_EMPTY after the first
-// round when `release_qkg` (the g tile's space is no longer read) and B_T at
-// the end.
-__device__ __forceinline__ bool ut_solve(const Ctx& X, const Lane& t, uint32_t tmem, int warp,
-                                         int step, bool release_qkg, uint8_t* t16_dst)
+// Sum over m < 16 of row[m] col[m] (row: 16 floats, 16-byte aligned).
+__device__ __forceinline__ float dot16(const float* row, const float (&col)[16])
+{
+    float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+    for (int m4 = 0; m4 < 4; ++m4) {
+        const float4 rv = *reinterpret_cast<const float4*>(row + 4 * m4);
+        a0 = fmaf(rv.x, col[4 * m4 + 0], a0);
+        a1 = fmaf(rv.y, col[4 * m4 + 1], a1);
+        a0 = fmaf(rv.z, col[4 * m4 + 2], a0);
+        a1 = fmaf(rv.w, col[4 * m4 + 3], a1);
+    }
+    return a0 + a1;
+}
+
+// A column of 16 floats, stride ld.
+__device__ __forceinline__ void load_col16(const float* p, int ld, float (&col)[16])
+{
+#pragma unroll
+    for (int m = 0; m < 16; ++m) col[m] = p[m * ld];
+}
+
+// Front phase 5: the UT solve, fp32 on the CUDA cores.  From A (OFF_A32)
+// builds X = (I + A)^{-1} (OFF_X) block by block and writes T = X Diag(b) as
+// the fp16 tile t16_dst ([r][i], zero above the diagonal; b = the masked beta
+// of the pass, so T is zero outside the pass).  Arrives B_T at the end.
+//
+// The block recurrence X_ij = -X_ii sum_{j<=k<i} A_ik X_kj runs in rounds;
+// thread (r, c) = (ct / 16, ct % 16) forms element (r, c) of every block
+// product of a round (Z and P: partial sums, Y: finished off-diagonal blocks):
+//   D   X_00 .. X_33 (64 threads, one column of one diagonal block each)
+//   1   Z10 = A10 X00   P20 = A20 X00   P30 = A30 X00   Z21 = A21 X11
+//       P31 = A31 X11   Z32 = A32 X22
+//   2   Y10 = -X11 Z10  Y21 = -X22 Z21  Y32 = -X33 Z32
+//   3   Z20 = P20 + A21 Y10   Z31 = P31 + A32 Y21   P30 += A31 Y10
+//   4   Y20 = -X22 Z20  Y31 = -X33 Z31
+//   5   Z30 = P30 + A32 Y20
+//   6   Y30 = -X33 Z30
+// P stays in the thread's registers; Z goes through OFF_ZS.
+__device__ __forceinline__ void ut_solve(const Ctx& X, const Lane& t, uint8_t* t16_dst)
 {
     uint8_t* sm = X.sm;
     const float* sBst = reinterpret_cast<const float*>(sm + OFF_BST);
     const float* sA = reinterpret_cast<const float*>(sm + OFF_A32);
-    float* sD = reinterpret_cast<float*>(sm + OFF_DF);
-    const int ct = t.ct, L = t.L, half = t.half;
-    const uint32_t lane_base = t.lane_base;
-    const bool top = (warp & 3) < 2;         // this warp holds rows 0..63
-    // S1a: diagonal-block inverses (warps of ct < 128, one column each): D
-    // in fp32 and D' = D Diag(b) as the K-major fp16 B tile.  Meanwhile the
-    // other warps fill the chunks of the N and I - N tiles that lie in
-    // diagonal or upper blocks (zero in N; identity or zero in I - N).
-    if (ct < 128) {
-        const int b = ct >> 5, j = ct & 31;
+    float* sX = reinterpret_cast<float*>(sm + OFF_X);
+    float* sZ = reinterpret_cast<float*>(sm + OFF_ZS);
+    const int ct = t.ct;
+    if (ct < 64) {
+        // Column j of the unit-lower diagonal block b, by forward substitution.
+        const int b = ct >> 4, j = ct & 15;
+        const float* L = sA + (16 * b) * LDA + 16 * b;
         float x[16];
-        diag_block_column(sA, b, j, x);
-        if (j < 16) {
-            const int k = 16 * b + j;        // column k of D = row k of the D' tile
-            const float bk = sBst[k];
 #pragma unroll
-            for (int r = 0; r < 16; ++r) sD[(16 * b + r) * 17 + j] = x[r];
+        for (int r = 0; r < 16; ++r) x[r] = (r == j) ? 1.f : 0.f;
 #pragma unroll
-            for (int c8 = 0; c8 < 8; ++c8) {
-                uint32_t pq[4];
+        for (int i = 0; i < 15; ++i)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    float dv[2];
+            for (int r = i + 1; r < 16; ++r) x[r] = fmaf(-L[r * LDA + i], x[i], x[r]);
+        float* xo = sX + (16 * b) * LDA + 16 * b + j;
 #pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int r = 8 * c8 + 2 * e + u;
-                        dv[u] = ((r >> 4) == b) ? x[r & 15] : 0.f;
-                    }
-                    pq[e] = pack_f16x2(dv[0] * bk, dv[1] * bk);
-                }
-                st_chunk(sm + OFF_DPK, k, c8, make_uint4(pq[0], pq[1], pq[2], pq[3]));
-            }
-        }
-    } else {
-        // row R, column blocks 2 jb .. 2 jb + 1 of 16 (chunks 4 jb .. 4 jb + 3)
-        const int R = (ct - 128) >> 1, jb = (ct - 128) & 1;
-#pragma unroll
-        for (int cb = 0; cb < 2; ++cb) {
-            const int blk16 = 2 * jb + cb;
-            if (blk16 >= (R >> 4)) {
-#pragma unroll
-                for (int h8 = 0; h8 < 2; ++h8) {
-                    const int chunk = 2 * blk16 + h8;
-                    st_chunk(sm + OFF_NB, R, chunk, make_uint4(0, 0, 0, 0));
-                    // the 1 of I - N: column R, in chunk R / 8 at position R % 8
-                    uint32_t w[4] = {0, 0, 0, 0};
-                    if (chunk == (R >> 3)) w[(R & 7) >> 1] = (R & 1) ? 0x3C000000u : 0x3C00u;
-                    st_chunk(sm + OFF_IMN, R, chunk, make_uint4(w[0], w[1], w[2], w[3]));
-                }
-            }
-        }
+        for (int r = 0; r < 16; ++r) xo[r * LDA] = x[r];
     }
     group_sync();
-    // S1b: N = D A_off, whose non-zero blocks are N_ij = D_ii A_ij for
-    // (i, j) = (1,0) (2,0) (2,1) (3,0) (3,1) (3,2): 6 x 16 rows x 8 column
-    // pairs = 768 segments, three per thread (computed together), written
-    // (fp16) to the N tile and, negated, to the I - N tile.  Both tiles serve
-    // as K-major A operands of the first product round (the N tile also as
-    // its MN-major B operand).
+    const int r = ct >> 4, c = ct & 15;
+    auto arow = [&](int bi, int bj) { return sA + (16 * bi + r) * LDA + 16 * bj; };
+    auto xrow = [&](int bi, int bj) { return sX + (16 * bi + r) * LDA + 16 * bj; };
+    auto xat = [&](int bi, int bj) -> float& { return sX[(16 * bi + r) * LDA + 16 * bj + c]; };
+    float col[16];
+    float p20, p30, p31;
+    // round 1
+    load_col16(sX + c, LDA, col);                                  // X00[:, c]
+    sZ[0 * 256 + r * 16 + c] = dot16(arow(1, 0), col);
+    p20 = dot16(arow(2, 0), col);
+    p30 = dot16(arow(3, 0), col);
+    load_col16(sX + 16 * LDA + 16 + c, LDA, col);                  // X11[:, c]
+    sZ[1 * 256 + r * 16 + c] = dot16(arow(2, 1), col);
+    p31 = dot16(arow(3, 1), col);
+    load_col16(sX + 32 * LDA + 32 + c, LDA, col);                  // X22[:, c]
+    sZ[2 * 256 + r * 16 + c] = dot16(arow(3, 2), col);
+    group_sync();
+    // round 2
     {
-        const float* drow[3];
-        const float* acol[3];
-        uint32_t off[3];
+        float y[3];
 #pragma unroll
-        for (int rep = 0; rep < 3; ++rep) {
-            const int sgi = ct + 256 * rep;
-            const int b6 = sgi >> 7, rr = (sgi >> 3) & 15, cpair = sgi & 7;
-            const int bi = (b6 == 0) ? 1 : ((b6 < 3) ? 2 : 3);
-            const int bj = (b6 == 0) ? 0 : ((b6 < 3) ? b6 - 1 : b6 - 3);
-            drow[rep] = sD + (16 * bi + rr) * 17;
-            acol[rep] = sA + (16 * bi) * LDA + 16 * bj + 2 * cpair;
-            const int R = 16 * bi + rr, col = 16 * bj + 2 * cpair, chunk = col >> 3;
-            off[rep] = (R >> 3) * 1024 + (R & 7) * 128 + ((chunk ^ (R & 7)) << 4) + (col & 7) * 2;
+        for (int k = 0; k < 3; ++k) {
+            load_col16(sZ + k * 256 + c, 16, col);
+            y[k] = -dot16(xrow(k + 1, k + 1), col);
         }
-        float n[3][2];
-#pragma unroll
-        for (int rep = 0; rep < 3; ++rep) n[rep][0] = n[rep][1] = 0.f;
-#pragma unroll
-        for (int m = 0; m < 16; ++m) {
-#pragma unroll
-            for (int rep = 0; rep < 3; ++rep) {
-                const float d = drow[rep][m];
-                const float2 a = *reinterpret_cast<const float2*>(acol[rep] + m * LDA);
-                n[rep][0] = fmaf(d, a.x, n[rep][0]);
-                n[rep][1] = fmaf(d, a.y, n[rep][1]);
-            }
-        }
-#pragma unroll
-        for (int rep = 0; rep < 3; ++rep) {
-            *reinterpret_cast<uint32_t*>(sm + OFF_NB + off[rep]) = pack_f16x2(n[rep][0], n[rep][1]);
-            *reinterpret_cast<uint32_t*>(sm + OFF_IMN + off[rep]) = pack_f16x2(-n[rep][0], -n[rep][1]);
-        }
+        xat(1, 0) = y[0];
+        xat(2, 1) = y[1];
+        xat(3, 2) = y[2];
     }
-    fence_proxy_async_smem();
     group_sync();
-    if (ct == 0) mbar_arrive(&X.bar[B_S1]);
-    // S2: Z -> fp16 MN-major B tile; I + N^2 -> fp16 A operand.
-    if (!group_wait(X, B_R1, step)) return false;
-    // The g tile's space (D, N, D' tiles) is no longer read: the next chunk may load.
-    if (ct == 0 && release_qkg) mbar_arrive(&X.bar[B_QKG_EMPTY]);
-    tc_fence_after();
-    if (top) {
-        uint32_t zb[16], d[32], ip[16];
-        tmem_row_f16(tmem + lane_base + TM_Z + 32 * half, zb);
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            st_chunk(sm + OFF_ZB, L, 4 * half + j,
-                     make_uint4(zb[4 * j], zb[4 * j + 1], zb[4 * j + 2], zb[4 * j + 3]));
-        tmem_ld32(tmem + lane_base + TM_N2 + 32 * half, d);
-        tmem_ld_wait();
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const int k = 32 * half + 2 * i;
-            const float a0 = __uint_as_float(d[2 * i]) + ((k == L) ? 1.f : 0.f);
-            const float a1 = __uint_as_float(d[2 * i + 1]) + ((k + 1 == L) ? 1.f : 0.f);
-            ip[i] = pack_f16x2(a0, a1);
-        }
-        tmem_st16(tmem + lane_base + TM_IPN + 16 * half, ip);
-        tmem_st_wait();
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
+    // round 3
+    load_col16(sX + 16 * LDA + c, LDA, col);                       // Y10[:, c]
+    const float z20 = p20 + dot16(arow(2, 1), col);
+    p30 += dot16(arow(3, 1), col);
+    load_col16(sX + 32 * LDA + 16 + c, LDA, col);                  // Y21[:, c]
+    const float z31 = p31 + dot16(arow(3, 2), col);
+    sZ[0 * 256 + r * 16 + c] = z20;
+    sZ[1 * 256 + r * 16 + c] = z31;
     group_sync();
-    if (ct == 0) mbar_arrive(&X.bar[B_S2]);
-    // S3: T -> bf16 (W product) and fp16 (V product) rows
-    if (!group_wait(X, B_R2, step)) return false;
-    tc_fence_after();
-    if (top) {
-        uint32_t d[32];
-        tmem_ld32(tmem + lane_base + TM_T + 32 * half, d);
-        tmem_ld_wait();
+    // round 4
+    load_col16(sZ + c, 16, col);
+    const float y20 = -dot16(xrow(2, 2), col);
+    load_col16(sZ + 256 + c, 16, col);
+    const float y31 = -dot16(xrow(3, 3), col);
+    xat(2, 0) = y20;
+    xat(3, 1) = y31;
+    group_sync();
+    // round 5
+    load_col16(sX + 32 * LDA + c, LDA, col);                       // Y20[:, c]
+    sZ[2 * 256 + r * 16 + c] = p30 + dot16(arow(3, 2), col);
+    group_sync();
+    // round 6
+    load_col16(sZ + 512 + c, 16, col);
+    xat(3, 0) = -dot16(xrow(3, 3), col);
+    group_sync();
+    // T = X Diag(b), fp16, zero above the diagonal: 512 chunks of 8, two per thread.
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            uint32_t pb[4], ph[4];
+    for (int e = 0; e < 2; ++e) {
+        const int q = ct + 256 * e, rr = q >> 3, j = q & 7;
+        const float4* xr = reinterpret_cast<const float4*>(sX + rr * LDA + 8 * j);
+        const float4* bb = reinterpret_cast<const float4*>(sBst + 8 * j);
+        const float4 x0 = xr[0], x1 = xr[1], b0 = bb[0], b1 = bb[1];
+        const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+        const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+        uint32_t pk[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float t0v = __uint_as_float(d[8 * j + 2 * e]);
-                const float t1v = __uint_as_float(d[8 * j + 2 * e + 1]);
-                pb[e] = pack_bf16x2(t0v, t1v);
-                ph[e] = pack_f16x2(t0v, t1v);
-            }
-            st_chunk(sm + OFF_T, L, 4 * half + j, make_uint4(pb[0], pb[1], pb[2], pb[3]));
-            st_chunk(t16_dst, L, 4 * half + j, make_uint4(ph[0], ph[1], ph[2], ph[3]));
+        for (int k = 0; k < 4; ++k) {
+            const int i0 = 8 * j + 2 * k;
+            pk[k] = pack_f16x2(i0 <= rr ? xv[2 * k] * bv[2 * k] : 0.f,
+                               i0 + 1 <= rr ? xv[2 * k + 1] * bv[2 * k + 1] : 0.f);
         }
+        st_chunk(t16_dst, rr, j, make_uint4(pk[0], pk[1], pk[2], pk[3]));
     }
-    fence_proxy_async_smem();
-    tc_fence_before();
+    fence_proxy_async_smem();      // T is read by the W product (and copied out)
     group_sync();
     if (ct == 0) mbar_arrive(&X.bar[B_T]);
-    return true;
 }
 
-// Front phase 6: W readout, -W^T row c = -2^R_c x (Kr^T T^T) row c, fp16 to
-// wt_dst.  Ends with a group barrier.
+// Front phase 6: W readout, -W^T (fp16 [ch][r]) to wt_dst.  Ends with a group
+// barrier.
 __device__ __forceinline__ bool w_readout(const Ctx& X, const Lane& t, uint32_t tmem, int step,
                                           uint8_t* wt_dst)
 {
     if (!group_wait(X, B_MMA_W, step)) return false;
     tc_fence_after();
-    const float* sR = reinterpret_cast<const float*>(X.sm + OFF_R);
     {
         uint32_t dw[32];
         tmem_ld32(tmem + t.lane_base + TM_W + 32 * t.half, dw);
         tmem_ld_wait();
-        const float sc = -sR[t.L];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             uint32_t pk[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e)
-                pk[e] = pack_f16x2(sc * __uint_as_float(dw[8 * j + 2 * e]),
-                                   sc * __uint_as_float(dw[8 * j + 2 * e + 1]));
+                pk[e] = pack_f16x2(-__uint_as_float(dw[8 * j + 2 * e]),
+                                   -__uint_as_float(dw[8 * j + 2 * e + 1]));
             st_chunk(wt_dst, t.L, 4 * t.half + j, make_uint4(pk[0], pk[1], pk[2], pk[3]));
         }
     }
@@ -917,69 +871,45 @@ __device__ __forceinline__ void state_store(const Lane& t, uint32_t tmem, float*
 }
 
 // ---------------------------------------------------------------------------
-// MMA warp (one thread).
+// MMA warp.
 
 struct FrontDescs {
-    uint64_t AD, ADLO, BDHL, ADK, T, NA, IMN, NB, DPK, ZB;
-    uint32_t id_g, id_w, id_mn, id_k64;
+    uint64_t GA, GB, WA, WB;
+    uint32_t id_g, id_w;
 };
 
-// Base descriptors; a K step advances the start address field (16-byte
-// units) by 128 for MN-major tiles, by 2 for K-major ones.
-__device__ __forceinline__ FrontDescs make_front_descs(uint8_t* sm)
+// Base descriptors (K-major, 128-byte swizzle); a K step of 32 bytes advances
+// the start address field (16-byte units) by 2 inside a swizzle row, and the
+// tf32 tiles move to the next 32-channel group every four steps.  gk_off is
+// where the (e^G K)^T tile lives.
+__device__ __forceinline__ FrontDescs make_front_descs(uint8_t* sm, uint32_t gk_off)
 {
     FrontDescs D;
-    D.id_g = make_idesc_bf16(128, 128, true, true);     // Gram
-    D.id_w = make_idesc_bf16(128, 64, false, false);    // W
-    D.id_mn = make_idesc_f16(128, 64, false, true);     // K-major A x MN-major B
-    D.id_k64 = make_idesc_f16(128, 64, false, false);   // K-major A x K-major B
-    D.AD = make_sdesc(smem_u32(sm + OFF_AD), 16384, 1024, kSwizzle128B);
-    D.ADLO = make_sdesc(smem_u32(sm + OFF_ADLO), 16384, 1024, kSwizzle128B);
-    D.BDHL = make_sdesc(smem_u32(sm + OFF_BD), OFF_BDLO - OFF_BD, 1024, kSwizzle128B);
-    D.ADK = make_sdesc(smem_u32(sm + OFF_AD), 16, 1024, kSwizzle128B);
-    D.T = make_sdesc(smem_u32(sm + OFF_T), 16, 1024, kSwizzle128B);
-    D.NA = make_sdesc(smem_u32(sm + OFF_NB), 16, 1024, kSwizzle128B);   // N as K-major A
-    D.IMN = make_sdesc(smem_u32(sm + OFF_IMN), 16, 1024, kSwizzle128B);
-    D.NB = make_sdesc(smem_u32(sm + OFF_NB), 8192, 1024, kSwizzle128B);
-    D.DPK = make_sdesc(smem_u32(sm + OFF_DPK), 16, 1024, kSwizzle128B);
-    D.ZB = make_sdesc(smem_u32(sm + OFF_ZB), 8192, 1024, kSwizzle128B);
+    D.id_g = make_idesc_tf32(128, 64);                  // [Kr; Qr] Kc^T
+    D.id_w = make_idesc_f16(128, 64, false, false);     // (e^G K)^T T^T
+    D.GA = make_sdesc(smem_u32(sm + OFF_A), 16, 1024, kSwizzle128B);
+    D.GB = make_sdesc(smem_u32(sm + OFF_KC), 16, 1024, kSwizzle128B);
+    D.WA = make_sdesc(smem_u32(sm + gk_off), 16, 1024, kSwizzle128B);
+    D.WB = make_sdesc(smem_u32(sm + OFF_T16), 16, 1024, kSwizzle128B);
     return D;
 }
 
-// The front products of one step, after B_OPS: the Gram, the two solve
-// rounds and W^T.  Called by the whole MMA warp.  Returns false if a wait
-// gave up.
+// The front products of one step, after B_OPS: the Gram, then (after the
+// solve) W^T.  Called by the whole MMA warp.  Returns false if a wait gave up.
 __device__ __forceinline__ bool mma_front(const Ctx& X, uint32_t tmem, const FrontDescs& D,
                                           int step)
 {
-    // Gram: [Kr; Qr] (MN-major A) x [Kc hi | Kc lo] (MN-major B, N = 128),
-    // K = 128 channels, hi and lo A parts: the readout adds the halves.
+    // Gram: [Kr; Qr] (M = 128) x Kc^T (N = 64), K = 128 channels in 16 tf32 steps.
 #pragma unroll
-    for (int s = 0; s < 8; ++s) mma_ss(tmem + TM_G, D.AD + 128 * s, D.BDHL + 128 * s, D.id_g, s > 0);
-#pragma unroll
-    for (int s = 0; s < 8; ++s) mma_ss(tmem + TM_G, D.ADLO + 128 * s, D.BDHL + 128 * s, D.id_g, 1);
+    for (int s = 0; s < 16; ++s)
+        mma_ss_tf32(tmem + TM_G, D.GA + (s >> 2) * (16384 >> 4) + (s & 3) * 2,
+                    D.GB + (s >> 2) * (8192 >> 4) + (s & 3) * 2, D.id_g, s > 0);
     mma_commit(&X.bar[B_MMA_G]);
-    // UT solve, round 1: N^2 = N N and Z = (I - N) D'; round 2: T = (I + N^2) Z.
-    if (!warp_wait(X, B_S1, step)) return false;
-    tc_fence_after();
-    // (M = 128 with A rows 64..127 read from the next tile: finite data,
-    // rows unused.)
-#pragma unroll
-    for (int s = 0; s < 4; ++s) mma_ss(tmem + TM_N2, D.NA + 2 * s, D.NB + 128 * s, D.id_mn, s > 0);
-#pragma unroll
-    for (int s = 0; s < 4; ++s) mma_ss(tmem + TM_Z, D.IMN + 2 * s, D.DPK + 2 * s, D.id_k64, s > 0);
-    mma_commit(&X.bar[B_R1]);
-    if (!warp_wait(X, B_S2, step)) return false;
-    tc_fence_after();
-#pragma unroll
-    for (int s = 0; s < 4; ++s)
-        mma_ts(tmem + TM_T, tmem + TM_IPN + 8 * s, D.ZB + 128 * s, D.id_mn, s > 0);
-    mma_commit(&X.bar[B_R2]);
     if (!warp_wait(X, B_T, step)) return false;
     tc_fence_after();
-    // W^T (unscaled) = Kr^T T^T: A = Kr hi as K-major [ch][tok], B = T [r][i].
+    // W^T = (e^G K)^T T^T: A = (e^G K)^T [ch][i], B = T [r][i], K = 64 tokens.
 #pragma unroll
-    for (int s = 0; s < 4; ++s) mma_ss(tmem + TM_W, D.ADK + 2 * s, D.T + 2 * s, D.id_w, s > 0);
+    for (int s = 0; s < 4; ++s) mma_ss(tmem + TM_W, D.WA + 2 * s, D.WB + 2 * s, D.id_w, s > 0);
     mma_commit(&X.bar[B_MMA_W]);
     return true;
 }
