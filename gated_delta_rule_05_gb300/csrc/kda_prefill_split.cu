@@ -225,6 +225,11 @@ __device__ __forceinline__ void consumer(const Ctx& X, uint32_t tmem, int warp, 
         }
     } else {
         // ------------------------------------------------ compute group
+        // Per step, on the chain: the previous step's O^T and the state read
+        // from tensor memory, the fp16 copy of the state (then the first
+        // product may start), U^T to fp16 (then the second).  While the first
+        // product runs: the previous O to o (staged, one TMA store), the
+        // decay of the state in place and the next chunk's v tile to fp16.
         const Lane t = make_lane(threadIdx.x - 64, warp, lane);
         const int seq_off = (cu != nullptr && snap.interval > 0) ? snap.offsets[n] : 0;
         state_load(t, tmem, S0, sbase);
@@ -233,40 +238,39 @@ __device__ __forceinline__ void consumer(const Ctx& X, uint32_t tmem, int warp, 
         prev.t0 = 0;
         prev.lo = prev.hi = 0;
         int step = 0;
-        // The O of a step is read from tensor memory before the next step's
-        // products start and stored while they run.
         auto store_prev_o = [&](const uint32_t (&dd)[32]) {
             const bool tma_out = (sizeof(TO) == 2) && prev.lo == 0 && prev.hi == kC;
             o_store<TO>(t, dd, tma_out, tm_o, sm + C_OST, o, (long long)prev.t0, prev.lo, prev.hi,
                         h, H);
         };
+        // The v tile of chunk cv to fp16, once it has landed.
+        auto convert_v = [&](int cv) -> bool {
+            const int vb = cv & (kVBufs - 1);
+            if (!group_wait(X, B_SV_FULL0 + vb, cv / kVBufs)) return false;
+            v_tile_to_f16(sm + C_V0 + vb * 16384, t.ct);
+            fence_proxy_async_smem();
+            return true;
+        };
+        if (alive) alive = convert_v(0);
         while (alive) {
             const int s = step & 1;
             if (!group_wait(X, B_ST_FULL0 + s, step >> 1)) { alive = false; break; }
             const StepDesc d = X.desc[s];
-            if (d.first_pass) {
-                const int vb = d.chunk & (kVBufs - 1);
-                if (!group_wait(X, B_SV_FULL0 + vb, d.chunk / kVBufs)) { alive = false; break; }
-                v_tile_to_f16(sm + C_V0 + vb * 16384, t.ct);
-            }
             uint32_t dd[32];
-            if (step > 0) {
-                if (!group_wait(X, B_MMA_OS, step - 1)) { alive = false; break; }
-                tc_fence_after();
-                o_load(t, tmem, dd);
-            } else {
-                tc_fence_after();
-            }
-            state_decay(t, tmem, reinterpret_cast<const float*>(sm + s * kStage + BLK_GL),
-                        d.first_pass ? snapshot_at(snap, d.chunk, eos - bos, seq_off, H, h)
-                                     : nullptr);
-            fence_proxy_async_smem();             // the converted v tile
+            if (step > 0 && !group_wait(X, B_MMA_OS, step - 1)) { alive = false; break; }
+            tc_fence_after();
+            if (step > 0) o_load(t, tmem, dd);
+            state_copy_f16(t, tmem, TM_SB,
+                           d.first_pass ? snapshot_at(snap, d.chunk, eos - bos, seq_off, H, h)
+                                        : nullptr);
             tc_fence_before();
             if (t.ct == 0) bulk_wait_group_read0();   // the O staging is free again
             group_sync();
             if (t.ct == 0) mbar_arrive(&X.bar[B_OPS]);
             if (step > 0) store_prev_o(dd);
             prev = d;
+            state_scale(t, tmem, reinterpret_cast<const float*>(sm + s * kStage + BLK_GL));
+            if (d.last_pass && d.chunk + 1 < nch && !convert_v(d.chunk + 1)) { alive = false; break; }
             if (!group_wait(X, B_MMA_C, step)) { alive = false; break; }
             tc_fence_after();
             u_to_f16(t, tmem);
@@ -286,6 +290,8 @@ __device__ __forceinline__ void consumer(const Ctx& X, uint32_t tmem, int warp, 
             store_prev_o(dd);
         }
         if (t.ct == 0) bulk_wait_group0();               // the last O store has landed
+        // (A wait that gave up has set the abort flag; a unit without chunks
+        // stores its S0.)
         if (!*reinterpret_cast<volatile int32_t*>(&X.misc->abort)) {
             if (S_final) state_store(t, tmem, S_final, sbase);
             float* last = snapshot_at(snap, nch, eos - bos, seq_off, H, h);

@@ -940,5 +940,54 @@ __device__ __forceinline__ void mma_back_os(uint32_t tmem, uint32_t p)
     for (int s = 0; s < 4; ++s) mma_ts(tmem + TM_O, tmem + TM_UB + s * 8, dPK + 2 * s, id_os, 1);
 }
 
+// ---------------------------------------------------------------------------
+// The split consumer's form of the state decay, in two halves: the fp16 copy
+// (the A operand of the step's first product, on the chain) and the decay of
+// the fp32 state in place (during the first product, which does not read it).
+
+// S^T fp16 copy into columns sb; when `snap` is not null the state (the state
+// at the chunk start) is also stored there ([d_k][d_v] fp32).  This thread: 64
+// channels of its TMEM lane.  No barrier.
+__device__ __forceinline__ void state_copy_f16(const Lane& t, uint32_t tmem, uint32_t sb, float* snap)
+{
+    const int c0 = 64 * t.half;
+    uint32_t r0[32], r1[32], b[16];
+    tmem_ld32(tmem + t.lane_base + TM_S + c0, r0);
+    tmem_ld32(tmem + t.lane_base + TM_S + c0 + 32, r1);
+    tmem_ld_wait();
+    if (snap != nullptr) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            snap[(long long)(c0 + i) * kD + t.L] = __uint_as_float(r0[i]);
+            snap[(long long)(c0 + 32 + i) * kD + t.L] = __uint_as_float(r1[i]);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        b[i] = pack_f16x2(__uint_as_float(r0[2 * i]), __uint_as_float(r0[2 * i + 1]));
+    tmem_st16(tmem + t.lane_base + sb + (c0 >> 1), b);
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        b[i] = pack_f16x2(__uint_as_float(r1[2 * i]), __uint_as_float(r1[2 * i + 1]));
+    tmem_st16(tmem + t.lane_base + sb + (c0 >> 1) + 16, b);
+    tmem_st_wait();
+}
+
+// S^T <- S^T Diag(e^{G_last}) in place.  No barrier.
+__device__ __forceinline__ void state_scale(const Lane& t, uint32_t tmem, const float* gl)
+{
+#pragma unroll
+    for (int jb = 0; jb < 2; ++jb) {
+        const int c0 = 64 * t.half + 32 * jb;
+        uint32_t r[32];
+        tmem_ld32(tmem + t.lane_base + TM_S + c0, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * gl[c0 + i]);
+        tmem_st32(tmem + t.lane_base + TM_S + c0, r);
+    }
+    tmem_st_wait();
+}
+
 }  // namespace tc
 }  // namespace kda
