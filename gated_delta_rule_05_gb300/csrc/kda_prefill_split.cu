@@ -228,8 +228,9 @@ __device__ __forceinline__ void consumer(const Ctx& X, uint32_t tmem, int warp, 
         // Per step, on the chain: the previous step's O^T and the state read
         // from tensor memory, the fp16 copy of the state (then the first
         // product may start), U^T to fp16 (then the second).  While the first
-        // product runs: the previous O to o (staged, one TMA store), the
-        // decay of the state in place and the next chunk's v tile to fp16.
+        // product runs: the previous O to o (staged, one TMA store) and the
+        // decay of the state in place; while the second runs, the next
+        // chunk's v tile to fp16.
         const Lane t = make_lane(threadIdx.x - 64, warp, lane);
         const int seq_off = (cu != nullptr && snap.interval > 0) ? snap.offsets[n] : 0;
         state_load(t, tmem, S0, sbase);
@@ -270,13 +271,13 @@ __device__ __forceinline__ void consumer(const Ctx& X, uint32_t tmem, int warp, 
             if (step > 0) store_prev_o(dd);
             prev = d;
             state_scale(t, tmem, reinterpret_cast<const float*>(sm + s * kStage + BLK_GL));
-            if (d.last_pass && d.chunk + 1 < nch && !convert_v(d.chunk + 1)) { alive = false; break; }
             if (!group_wait(X, B_MMA_C, step)) { alive = false; break; }
             tc_fence_after();
             u_to_f16(t, tmem);
             tc_fence_before();
             group_sync();
             if (t.ct == 0) mbar_arrive(&X.bar[B_U]);
+            if (d.last_pass && d.chunk + 1 < nch && !convert_v(d.chunk + 1)) { alive = false; break; }
             ++step;
             if (d.last_step) break;
         }
