@@ -302,7 +302,7 @@ __device__ __forceinline__ void consumer(const Ctx& X, uint32_t tmem, int warp, 
 }
 
 // ------------------------------------------------------------- producer
-template <bool FUSED>
+template <typename TO, bool FUSED>
 __device__ __forceinline__ void producer(const Ctx& X, uint32_t tmem, int warp, int lane,
                                          const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                                          const CUtensorMap* tm_g, const float* beta,
@@ -470,7 +470,7 @@ __device__ __forceinline__ void producer(const Ctx& X, uint32_t tmem, int warp, 
                 }
                 group_sync();
                 pass_factors(X, t, ps, reinterpret_cast<float*>(sm + OFF_GL));
-                gram_operands<FUSED>(X, t, ps, Gq, sm + OFF_QG, sm + OFF_KT, sm + P_GK);
+                gram_operands<FUSED, sizeof(TO) == 4>(X, t, ps, Gq, sm + OFF_QG, sm + OFF_KT, sm + P_GK);
                 fence_proxy_async_smem();
                 group_sync();
                 if (ct == 0) {
@@ -562,7 +562,7 @@ prefill_split_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         consumer<TO>(X, tmem, warp, lane, &tm_v, &tm_o, S0, cu, ws, total_tokens, H, o, S_final, U,
                      R, flags, ring, snap);
     else
-        producer<FUSED>(X, tmem, warp, lane, &tm_q, &tm_k, &tm_g, beta, cu, ws, total_tokens, H, U,
+        producer<TO, FUSED>(X, tmem, warp, lane, &tm_q, &tm_k, &tm_g, beta, cu, ws, total_tokens, H, U,
                         R, flags, ring, gate);
 
     tc_fence_before();

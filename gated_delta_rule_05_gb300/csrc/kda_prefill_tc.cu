@@ -242,7 +242,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 // operand region.  The (e^G K)^T tile takes the g tile's place.
                 if (ct == 0) bulk_wait_group_read0();
                 group_sync();
-                gram_operands<FUSED>(X, t, ps, Gq, sm + OFF_QG, sm + OFF_KT, sm + OFF_G);
+                gram_operands<FUSED, sizeof(TO) == 4>(X, t, ps, Gq, sm + OFF_QG, sm + OFF_KT, sm + OFF_G);
                 fence_proxy_async_smem();
                 group_sync();
                 if (ct == 0) mbar_arrive(&X.bar[B_OPS]);

@@ -31,8 +31,11 @@
 // overflow; they are discarded by selection.
 //
 // Operand precision.  The Gram operands carry the exponent factors and need an
-// 8-bit exponent: they are fp32 values multiplied as tf32 (10-bit mantissa,
-// fp32 accumulation).  T, P, U, S, V, W, e^G Q, e^G K and Ktil are O(1) and
+// 8-bit exponent: they are fp32 values multiplied as tf32 (10-bit mantissa)
+// with fp32 accumulation.  With fp32 output they are rounded to nearest
+// first; with bf16 output the tensor cores' truncation is left in place (its
+// bias stays well below the output's own rounding, and the rounding costs
+// several percent of the launch).  T, P, U, S, V, W, e^G Q, e^G K and Ktil are O(1) and
 // enter the tensor cores as fp16 (3 more mantissa bits than bf16).  The UT
 // solve runs in fp32 and the state is carried in fp32.  |v| and the state
 // entries are assumed to stay inside the fp16 range (|x| < 65504).
@@ -160,6 +163,16 @@ __device__ __forceinline__ float ex2(float x)
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// x as a tf32 operand rounded to nearest: the tensor cores read only the top
+// 19 bits (sign, exponent, 10 mantissa bits) and would otherwise truncate,
+// a bias of the same sign on every operand.  Adding half a unit of the 10th
+// mantissa bit to the bit pattern rounds the magnitude to nearest (a carry
+// into the exponent is the correct result); the low 13 bits are ignored.
+__device__ __forceinline__ float tf32_round(float x)
+{
+    return __uint_as_float(__float_as_uint(x) + 0x1000u);
 }
 
 __device__ __forceinline__ float lo_bf16(uint32_t x) { return __uint_as_float(x << 16); }
@@ -419,8 +432,9 @@ __device__ __forceinline__ uint32_t tf32_kmajor(int row, int ch, uint32_t kstrid
 // 128-byte rows); the fp16 chunks of the two channels are stored in an order
 // that alternates between lane groups, so that a warp's 16-byte stores spread
 // over all eight swizzle positions.  With the gate prologue (FUSED) q and k
-// are scaled by their rows' inverse norms (OFF_NRM).  No barrier.
-template <bool FUSED>
+// are scaled by their rows' inverse norms (OFF_NRM).  ROUND: the tf32
+// operands are rounded to nearest (see the precision note above).  No barrier.
+template <bool FUSED, bool ROUND>
 __device__ __forceinline__ void gram_operands(const Ctx& X, const Lane& t, const Pass& ps,
                                               const float2 (&Gq)[16], uint8_t* qg_dst,
                                               uint8_t* kt_dst, uint8_t* gk_dst)
@@ -465,12 +479,13 @@ __device__ __forceinline__ void gram_operands(const Ctx& X, const Lane& t, const
                     vq[u][w] = qq * e1;
                     vc[u][w] = kk * e2;
                 }
+                auto rnd = [](float x) { return ROUND ? tf32_round(x) : x; };
                 *reinterpret_cast<float2*>(sA + tf32_kmajor(r, 2 * cp, 16384)) =
-                    make_float2(vk[0][w], vk[1][w]);
+                    make_float2(rnd(vk[0][w]), rnd(vk[1][w]));
                 *reinterpret_cast<float2*>(sA + tf32_kmajor(64 + r, 2 * cp, 16384)) =
-                    make_float2(vq[0][w], vq[1][w]);
+                    make_float2(rnd(vq[0][w]), rnd(vq[1][w]));
                 *reinterpret_cast<float2*>(sKc + tf32_kmajor(r, 2 * cp, 8192)) =
-                    make_float2(vc[0][w], vc[1][w]);
+                    make_float2(rnd(vc[0][w]), rnd(vc[1][w]));
             }
 #pragma unroll
             for (int u = 0; u < 2; ++u) {

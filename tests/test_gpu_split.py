@@ -109,6 +109,15 @@ def test_split_all_wide(kda):
     check(kda, inp)
 
 
+def test_split_all_wide_fp32_output(kda):
+    # fp32 output shows the products' rounding without the bf16 output
+    # rounding on top; g = -5 makes every chunk two-pass, with the largest
+    # Gram factors.
+    inp = synth.generate([2000, 333], 4, 128, 128, dtype="bf16", s0_std=0.05, seed=7,
+                         gate_shift=-5.0)
+    check(kda, inp, o_dtype=torch.float32)
+
+
 def test_split_back_to_back_reuses_workspace(kda):
     # Two calls on one workspace: the work-list kernel clears the hand-over
     # flags and counters in between.
