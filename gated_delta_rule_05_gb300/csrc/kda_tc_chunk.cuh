@@ -64,10 +64,6 @@ constexpr int kC = 64;
 constexpr int kD = 128;
 constexpr int kGroup = 256;            // compute group: 8 warps
 constexpr int kGroupBar = 1;           // its named barrier
-// Named barriers of the UT solve's warp chains (producer warp arrives, the
-// warps that need its block wait): Y10 (chain 0 -> chains 1, 2), Y20
-// (chain 1 -> chain 2), Y21 (chain 3 -> chain 4).
-constexpr int kBarY10 = 2, kBarY20 = 3, kBarY21 = 4;
 constexpr float kLog2e = 1.4426950408889634f;
 // Largest decay span (log2 units) handled in one pass.
 constexpr float kSpanMax = 250.f;
@@ -84,9 +80,8 @@ constexpr uint32_t OFF_KC = 147456;    // Gram B operand Kc tf32, K-major [64][1
 // After the Gram product, in the operand region [OFF_A, OFF_QG):
 constexpr uint32_t OFF_A32 = OFF_A;           // A fp32 [64][LDA]
 constexpr uint32_t OFF_X = OFF_A + 17408;     // X = (I + A)^-1 fp32 [64][LDA]
-constexpr uint32_t OFF_ZS = OFF_X + 17408;    // solve scratch, 6 x [16][24] fp32 (one per warp chain);
-constexpr uint32_t OFF_STAT = OFF_ZS;         //   during gate prep: decay stats fp32 [3][4][128]
-constexpr int LDZ = 24;                       // row stride (floats) of a chain's scratch block
+constexpr uint32_t OFF_ZS = OFF_X + 17408;    // solve scratch, 3 x [16][16] fp32
+constexpr uint32_t OFF_STAT = OFF_ZS + 3072;  // gate prep: decay stats fp32 [3][4][128]
 constexpr uint32_t OFF_T16 = 126976;   // T       [r][i] fp16 (W and V products)
 constexpr uint32_t OFF_WT = 163840;    // -W^T    [ch][r] fp16 (directly before (e^G Q)^T)
 constexpr uint32_t OFF_QG = 180224;    // (e^G Q)^T [ch][r] fp16
@@ -105,8 +100,7 @@ constexpr uint32_t OFF_MISC = 224544;  // tmem base, flags
 constexpr uint32_t kSmemUsed = 224560;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;   // + alignment slack
 constexpr int LDA = 68;                // row stride (floats) of A / X: 16-byte aligned rows
-static_assert(OFF_ZS + 6 * 16 * 24 * 4 <= OFF_T16 && OFF_STAT + 6144 <= OFF_T16 &&
-              OFF_T16 + 8192 <= OFF_WT, "post-Gram tiles overlap");
+static_assert(OFF_STAT + 6144 <= OFF_T16 && OFF_T16 + 8192 <= OFF_WT, "post-Gram tiles overlap");
 static_assert(OFF_KC + 32768 == OFF_QG && OFF_A + 65536 == OFF_KC, "operand region");
 static_assert(OFF_QG - OFF_WT == 16384 && OFF_KT - OFF_P == 8192,
               "the back products read -W^T | (e^G Q)^T and P | Ktil^T as one tile each");
@@ -573,63 +567,26 @@ __device__ __forceinline__ bool gram_readout(const Ctx& X, const Lane& t, uint32
     return true;
 }
 
-// m16n8k8 tf32 warp MMA, fp32 accumulate: c += a b.
-__device__ __forceinline__ void mma_tf32_m16n8k8(float (&c)[4], const uint32_t (&a)[4],
-                                                 const uint32_t (&b)[2])
+// Sum over m < 16 of row[m] col[m] (row: 16 floats, 16-byte aligned).
+__device__ __forceinline__ float dot16(const float* row, const float (&col)[16])
 {
-    asm volatile(
-        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7},"
-        " {%8, %9}, {%0, %1, %2, %3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
-}
-
-// x = hi + lo with hi and lo tf32 values (hi rounded to nearest, lo the rest
-// rounded): three tf32 products hi.hi + hi.lo + lo.hi carry about 21 bits.
-__device__ __forceinline__ void tf32_split(float x, uint32_t& hi, uint32_t& lo)
-{
-    hi = (__float_as_uint(x) + 0x1000u) & 0xFFFFE000u;
-    lo = (__float_as_uint(x - __uint_as_float(hi)) + 0x1000u) & 0xFFFFE000u;
-}
-
-// One warp's 16 x 16 block product c += (sL Lb) Rb in fp32-equivalent
-// precision (three tf32 warp MMAs per 8 x 8 x 8 piece).  Lb, Rb: fp32 blocks
-// with row strides ldl, ldr.  c[nh] is the m16n8 accumulator fragment of
-// columns 8nh .. 8nh+7: lane (g, t) = (lane / 4, lane % 4) holds rows g and
-// g + 8, columns 8nh + 2t and 8nh + 2t + 1.
-__device__ __forceinline__ void blk_mma(const float* Lb, int ldl, const float* Rb, int ldr, int lane,
-                                        float sL, float (&c)[2][4])
-{
-    const int g = lane >> 2, t = lane & 3;
+    float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-    for (int ks = 0; ks < 2; ++ks) {
-        const int k0 = 8 * ks + t;
-        const float av[4] = {sL * Lb[g * ldl + k0], sL * Lb[(g + 8) * ldl + k0],
-                             sL * Lb[g * ldl + k0 + 4], sL * Lb[(g + 8) * ldl + k0 + 4]};
-        uint32_t ahi[4], alo[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) tf32_split(av[i], ahi[i], alo[i]);
-#pragma unroll
-        for (int nh = 0; nh < 2; ++nh) {
-            uint32_t bhi[2], blo[2];
-            tf32_split(Rb[k0 * ldr + 8 * nh + g], bhi[0], blo[0]);
-            tf32_split(Rb[(k0 + 4) * ldr + 8 * nh + g], bhi[1], blo[1]);
-            mma_tf32_m16n8k8(c[nh], alo, bhi);
-            mma_tf32_m16n8k8(c[nh], ahi, blo);
-            mma_tf32_m16n8k8(c[nh], ahi, bhi);
-        }
+    for (int m4 = 0; m4 < 4; ++m4) {
+        const float4 rv = *reinterpret_cast<const float4*>(row + 4 * m4);
+        a0 = fmaf(rv.x, col[4 * m4 + 0], a0);
+        a1 = fmaf(rv.y, col[4 * m4 + 1], a1);
+        a0 = fmaf(rv.z, col[4 * m4 + 2], a0);
+        a1 = fmaf(rv.w, col[4 * m4 + 3], a1);
     }
+    return a0 + a1;
 }
 
-// Stores a warp's accumulator block (fragment layout of blk_mma).
-__device__ __forceinline__ void blk_store(float* D, int ldd, int lane, const float (&c)[2][4])
+// A column of 16 floats, stride ld.
+__device__ __forceinline__ void load_col16(const float* p, int ld, float (&col)[16])
 {
-    const int g = lane >> 2, t = lane & 3;
 #pragma unroll
-    for (int nh = 0; nh < 2; ++nh) {
-        *reinterpret_cast<float2*>(D + g * ldd + 8 * nh + 2 * t) = make_float2(c[nh][0], c[nh][1]);
-        *reinterpret_cast<float2*>(D + (g + 8) * ldd + 8 * nh + 2 * t) = make_float2(c[nh][2], c[nh][3]);
-    }
+    for (int m = 0; m < 16; ++m) col[m] = p[m * ld];
 }
 
 // Front phase 5: the UT solve, fp32 on the CUDA cores.  From A (OFF_A32)
@@ -637,27 +594,25 @@ __device__ __forceinline__ void blk_store(float* D, int ldd, int lane, const flo
 // the fp16 tile t16_dst ([r][i], zero above the diagonal; b = the masked beta
 // of the pass, so T is zero outside the pass).  Arrives B_T at the end.
 //
-// The diagonal blocks' inverses X_bb come first (64 threads, one column of one
-// block each, by forward substitution).  The off-diagonal blocks
-// X_ij = -X_ii sum_{j<=k<i} A_ik X_kj then form six chains, one warp each,
-// every block product a warp's 16 x 16 product on the tensor cores (blk_mma,
-// split tf32 for fp32 accuracy); partial sums stay in the accumulator
-// fragments and a chain's intermediate block goes through its own scratch
-// block in OFF_ZS:
-//   chain 0   Y10 = -X11 (A10 X00)
-//   chain 1   Y20 = -X22 (A20 X00 + A21 Y10)               waits for Y10
-//   chain 2   Y30 = -X33 (A30 X00 + A31 Y10 + A32 Y20)     waits for Y10, Y20
-//   chain 3   Y21 = -X22 (A21 X11)
-//   chain 4   Y31 = -X33 (A31 X11 + A32 Y21)               waits for Y21
-//   chain 5   Y32 = -X33 (A32 X22)
-// A chain that others wait for signals its block with a named-barrier arrive
-// (kBarY10, kBarY20, kBarY21).
+// The block recurrence X_ij = -X_ii sum_{j<=k<i} A_ik X_kj runs in rounds;
+// thread (r, c) = (ct / 16, ct % 16) forms element (r, c) of every block
+// product of a round (Z and P: partial sums, Y: finished off-diagonal blocks):
+//   D   X_00 .. X_33 (64 threads, one column of one diagonal block each)
+//   1   Z10 = A10 X00   P20 = A20 X00   P30 = A30 X00   Z21 = A21 X11
+//       P31 = A31 X11   Z32 = A32 X22
+//   2   Y10 = -X11 Z10  Y21 = -X22 Z21  Y32 = -X33 Z32
+//   3   Z20 = P20 + A21 Y10   Z31 = P31 + A32 Y21   P30 += A31 Y10
+//   4   Y20 = -X22 Z20  Y31 = -X33 Z31
+//   5   Z30 = P30 + A32 Y20
+//   6   Y30 = -X33 Z30
+// P stays in the thread's registers; Z goes through OFF_ZS.
 __device__ __forceinline__ void ut_solve(const Ctx& X, const Lane& t, uint8_t* t16_dst)
 {
     uint8_t* sm = X.sm;
     const float* sBst = reinterpret_cast<const float*>(sm + OFF_BST);
     const float* sA = reinterpret_cast<const float*>(sm + OFF_A32);
     float* sX = reinterpret_cast<float*>(sm + OFF_X);
+    float* sZ = reinterpret_cast<float*>(sm + OFF_ZS);
     const int ct = t.ct;
     if (ct < 64) {
         // Column j of the unit-lower diagonal block b, by forward substitution.
@@ -675,61 +630,60 @@ __device__ __forceinline__ void ut_solve(const Ctx& X, const Lane& t, uint8_t* t
         for (int r = 0; r < 16; ++r) xo[r * LDA] = x[r];
     }
     group_sync();
-    const int wc = ct >> 5, lane = ct & 31;
-    auto Ab = [&](int bi, int bj) { return sA + (16 * bi) * LDA + 16 * bj; };
-    auto Xb = [&](int bi, int bj) { return sX + (16 * bi) * LDA + 16 * bj; };
-    float* Z = reinterpret_cast<float*>(sm + OFF_ZS) + 16 * LDZ * wc;
-    float acc[2][4];
-    auto zero = [&]() {
+    const int r = ct >> 4, c = ct & 15;
+    auto arow = [&](int bi, int bj) { return sA + (16 * bi + r) * LDA + 16 * bj; };
+    auto xrow = [&](int bi, int bj) { return sX + (16 * bi + r) * LDA + 16 * bj; };
+    auto xat = [&](int bi, int bj) -> float& { return sX[(16 * bi + r) * LDA + 16 * bj + c]; };
+    float col[16];
+    float p20, p30, p31;
+    // round 1
+    load_col16(sX + c, LDA, col);                                  // X00[:, c]
+    sZ[0 * 256 + r * 16 + c] = dot16(arow(1, 0), col);
+    p20 = dot16(arow(2, 0), col);
+    p30 = dot16(arow(3, 0), col);
+    load_col16(sX + 16 * LDA + 16 + c, LDA, col);                  // X11[:, c]
+    sZ[1 * 256 + r * 16 + c] = dot16(arow(2, 1), col);
+    p31 = dot16(arow(3, 1), col);
+    load_col16(sX + 32 * LDA + 32 + c, LDA, col);                  // X22[:, c]
+    sZ[2 * 256 + r * 16 + c] = dot16(arow(3, 2), col);
+    group_sync();
+    // round 2
+    {
+        float y[3];
 #pragma unroll
-        for (int i = 0; i < 2; ++i)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) acc[i][c] = 0.f;
-    };
-    // The chain's last step: Y = -X_ii Z (Z in this warp's scratch) into block (i, j).
-    auto finish = [&](int i, int j) {
-        blk_store(Z, LDZ, lane, acc);
-        __syncwarp();
-        zero();
-        blk_mma(Xb(i, i), LDA, Z, LDZ, lane, -1.f, acc);
-        blk_store(Xb(i, j), LDA, lane, acc);
-    };
-    if (wc == 0) {
-        zero();
-        blk_mma(Ab(1, 0), LDA, Xb(0, 0), LDA, lane, 1.f, acc);
-        finish(1, 0);
-        named_bar_arrive(kBarY10, 96);
-    } else if (wc == 1) {
-        zero();
-        blk_mma(Ab(2, 0), LDA, Xb(0, 0), LDA, lane, 1.f, acc);
-        named_bar_sync(kBarY10, 96);
-        blk_mma(Ab(2, 1), LDA, Xb(1, 0), LDA, lane, 1.f, acc);
-        finish(2, 0);
-        named_bar_arrive(kBarY20, 64);
-    } else if (wc == 2) {
-        zero();
-        blk_mma(Ab(3, 0), LDA, Xb(0, 0), LDA, lane, 1.f, acc);
-        named_bar_sync(kBarY10, 96);
-        blk_mma(Ab(3, 1), LDA, Xb(1, 0), LDA, lane, 1.f, acc);
-        named_bar_sync(kBarY20, 64);
-        blk_mma(Ab(3, 2), LDA, Xb(2, 0), LDA, lane, 1.f, acc);
-        finish(3, 0);
-    } else if (wc == 3) {
-        zero();
-        blk_mma(Ab(2, 1), LDA, Xb(1, 1), LDA, lane, 1.f, acc);
-        finish(2, 1);
-        named_bar_arrive(kBarY21, 64);
-    } else if (wc == 4) {
-        zero();
-        blk_mma(Ab(3, 1), LDA, Xb(1, 1), LDA, lane, 1.f, acc);
-        named_bar_sync(kBarY21, 64);
-        blk_mma(Ab(3, 2), LDA, Xb(2, 1), LDA, lane, 1.f, acc);
-        finish(3, 1);
-    } else if (wc == 5) {
-        zero();
-        blk_mma(Ab(3, 2), LDA, Xb(2, 2), LDA, lane, 1.f, acc);
-        finish(3, 2);
+        for (int k = 0; k < 3; ++k) {
+            load_col16(sZ + k * 256 + c, 16, col);
+            y[k] = -dot16(xrow(k + 1, k + 1), col);
+        }
+        xat(1, 0) = y[0];
+        xat(2, 1) = y[1];
+        xat(3, 2) = y[2];
     }
+    group_sync();
+    // round 3
+    load_col16(sX + 16 * LDA + c, LDA, col);                       // Y10[:, c]
+    const float z20 = p20 + dot16(arow(2, 1), col);
+    p30 += dot16(arow(3, 1), col);
+    load_col16(sX + 32 * LDA + 16 + c, LDA, col);                  // Y21[:, c]
+    const float z31 = p31 + dot16(arow(3, 2), col);
+    sZ[0 * 256 + r * 16 + c] = z20;
+    sZ[1 * 256 + r * 16 + c] = z31;
+    group_sync();
+    // round 4
+    load_col16(sZ + c, 16, col);
+    const float y20 = -dot16(xrow(2, 2), col);
+    load_col16(sZ + 256 + c, 16, col);
+    const float y31 = -dot16(xrow(3, 3), col);
+    xat(2, 0) = y20;
+    xat(3, 1) = y31;
+    group_sync();
+    // round 5
+    load_col16(sX + 32 * LDA + c, LDA, col);                       // Y20[:, c]
+    sZ[2 * 256 + r * 16 + c] = p30 + dot16(arow(3, 2), col);
+    group_sync();
+    // round 6
+    load_col16(sZ + 512 + c, 16, col);
+    xat(3, 0) = -dot16(xrow(3, 3), col);
     group_sync();
     // T = X Diag(b), fp16, zero above the diagonal: 512 chunks of 8, two per thread.
 #pragma unroll
