@@ -112,13 +112,16 @@ kda_status_t kda_prefill_host(const void* q, const void* k, const void* v, const
         return KDA_OK;
     }
 
-    cudaEvent_t ev_in[2], ev_comp[2], ev_out[2];
-    for (int s = 0; s < 2; ++s) {
-        if (cudaEventCreateWithFlags(&ev_in[s], cudaEventDisableTiming) != cudaSuccess ||
-            cudaEventCreateWithFlags(&ev_comp[s], cudaEventDisableTiming) != cudaSuccess ||
-            cudaEventCreateWithFlags(&ev_out[s], cudaEventDisableTiming) != cudaSuccess)
+    cudaEvent_t ev[6] = {};
+    for (int i = 0; i < 6; ++i) {
+        if (cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming) != cudaSuccess) {
+            for (int j = 0; j < i; ++j) cudaEventDestroy(ev[j]);
             return KDA_ERR_CUDA;
+        }
     }
+    cudaEvent_t* ev_in = ev;           // [2]: a slot's inputs are in
+    cudaEvent_t* ev_comp = ev + 2;     // [2]: a slot's compute is done
+    cudaEvent_t* ev_out = ev + 4;      // [2]: a slot's output has left
     kda_status_t st = KDA_OK;
     // Work already on `compute` (a previous call still reading the staging
     // slots, or the caller's producers of S0) precedes the first copy in.
@@ -162,11 +165,7 @@ kda_status_t kda_prefill_host(const void* q, const void* k, const void* v, const
     // The compute stream completes only after the last copy out.
     if (st == KDA_OK && err == cudaSuccess)
         err = cudaStreamWaitEvent(compute, ev_out[(nseg - 1) & 1], 0);
-    for (int s = 0; s < 2; ++s) {
-        cudaEventDestroy(ev_in[s]);
-        cudaEventDestroy(ev_comp[s]);
-        cudaEventDestroy(ev_out[s]);
-    }
+    for (int i = 0; i < 6; ++i) cudaEventDestroy(ev[i]);
     if (st != KDA_OK) return st;
     return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
