@@ -371,6 +371,16 @@ __device__ __forceinline__ void producer(const Ctx& X, uint32_t tmem, int warp, 
             bos = __shfl_sync(0xffffffffu, bos, 0);
             eos = __shfl_sync(0xffffffffu, eos, 0);
             const long long t0 = bos + (long long)c * kC;
+            // The tiles are requested first; the barrier's single arrival
+            // follows once beta (and A) are in shared memory, so the phase
+            // completes only when both have landed.
+            if (lane == 0) {
+                mbar_expect_tx(&X.bar[B_QKG_FULL], 2 * 16384 + 32768);
+                tma_load_2d(sm + OFF_Q, tm_q, hh * kD, (int32_t)t0, &X.bar[B_QKG_FULL]);
+                tma_load_2d(sm + OFF_K, tm_k, hh * kD, (int32_t)t0, &X.bar[B_QKG_FULL]);
+                tma_load_2d(sm + OFF_G, tm_g, hh * kD, (int32_t)t0, &X.bar[B_QKG_FULL]);
+                ++issued;
+            }
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
                 const int r = lane * 2 + j;
@@ -390,11 +400,7 @@ __device__ __forceinline__ void producer(const Ctx& X, uint32_t tmem, int warp, 
                 j.h = hh;
                 j.npass = 1;
                 j.terminate = 0;
-                mbar_arrive_expect_tx(&X.bar[B_QKG_FULL], 2 * 16384 + 32768);
-                tma_load_2d(sm + OFF_Q, tm_q, hh * kD, (int32_t)t0, &X.bar[B_QKG_FULL]);
-                tma_load_2d(sm + OFF_K, tm_k, hh * kD, (int32_t)t0, &X.bar[B_QKG_FULL]);
-                tma_load_2d(sm + OFF_G, tm_g, hh * kD, (int32_t)t0, &X.bar[B_QKG_FULL]);
-                ++issued;
+                mbar_arrive(&X.bar[B_QKG_FULL]);
                 if (jc > 0) ok = publish(jc - 1);
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);

@@ -17,7 +17,8 @@
 // are described with the phases in kda_tc_chunk.cuh.
 //
 // CTA roles (320 threads):
-//   warp 0      TMA: q, k, g tiles (64 x 128) and the v tile, beta by plain loads
+//   warp 0      TMA: q, k, g tiles (64 x 128) and the v tile, beta by plain
+//               loads one chunk ahead, the next chunk's tiles prefetched to L2
 //   warp 1      issues every tcgen05.mma and commit (warp-wide, one elected lane)
 //   warps 2..9  the compute group (256 threads) runs every CUDA-core phase of a
 //               chunk together: gate prep, state decay, Gram readout, the UT
@@ -144,19 +145,30 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         }
         float* sBin = reinterpret_cast<float*>(sm + OFF_BIN);
         int issued_qkg = 0, issued_v = 0;
+        // Each lane's two beta values are loaded one chunk ahead, so that
+        // their latency passes while the tiles are still in use; the next
+        // chunk's tiles are prefetched into L2 for the same reason.  Both keep
+        // plain global latency off the step between one chunk's W product and
+        // the next chunk's gate prep.
+        float b_next[2];
+        auto load_beta = [&](int ch, float* b) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const long long t = bos + (long long)ch * kC + lane * 2 + j;
+                b[j] = (t < eos) ? beta[t * H + h] : 0.f;
+            }
+        };
+        if (nch > 0) load_beta(0, b_next);
         for (int ch = 0; ch < nch; ++ch) {
             const long long t0 = bos + (long long)ch * kC;
             int ok = 1;
             if (lane == 0 && ch > 0) ok = wait_bar(X, B_QKG_EMPTY, ch - 1);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const int r = lane * 2 + j;
-                const long long t = t0 + r;
-                sBin[r] = (t < eos) ? beta[t * H + h] : 0.f;
-            }
+            sBin[lane * 2] = b_next[0];
+            sBin[lane * 2 + 1] = b_next[1];
             __syncwarp();
+            if (ch + 1 < nch) load_beta(ch + 1, b_next);
             if (lane == 0) {
                 mbar_arrive_expect_tx(&X.bar[B_QKG_FULL], 2 * 16384 + 32768);
                 tma_load_2d(sm + OFF_Q, &tm_q, h * kD, (int32_t)t0, &X.bar[B_QKG_FULL]);
@@ -170,6 +182,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     tma_load_2d(sm + OFF_V + 8192, &tm_v, h * kD + 64, (int32_t)t0,
                                 &X.bar[B_V_FULL]);
                     ++issued_v;
+                }
+                if (ok && ch + 1 < nch) {
+                    const int32_t tn = (int32_t)(t0 + kC);
+                    tma_prefetch_l2_2d(&tm_q, h * kD, tn);
+                    tma_prefetch_l2_2d(&tm_k, h * kD, tn);
+                    tma_prefetch_l2_2d(&tm_g, h * kD, tn);
+                    tma_prefetch_l2_2d(&tm_v, h * kD, tn);
+                    tma_prefetch_l2_2d(&tm_v, h * kD + 64, tn);
                 }
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);
