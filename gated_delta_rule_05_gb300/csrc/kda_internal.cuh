@@ -52,7 +52,11 @@ struct SplitPlan {
     size_t flags_off, ring_off, bytes;
 };
 
+// The producers keep each sequence's token range in shared memory.
+constexpr int kSplitMaxSeqs = 128;
+
 inline bool split_plan(int32_t num_seqs, int32_t H, int sms, SplitPlan* plan) {
+    if (num_seqs > kSplitMaxSeqs) return false;
     if (num_seqs < 1 || H < 1 || sms < 3) return false;
     const long long units = (long long)num_seqs * H;
     if (units > sms / 2) return false;

@@ -23,7 +23,7 @@
 // swizzled layout of the MMA descriptors, and e^{G_last}) straight from
 // registers into slot c mod R of the unit's ring in the workspace; a chunk
 // whose decay span needs two passes fills two step blocks.  The producer's
-// data-movement warp then publishes the slot: fence, then a release store of
+// data-movement warp then publishes the slot with a release store of
 // full[u][slot] = 2 (c + 1) + (passes - 1).  The consumer's loader polls that
 // word with acquire loads, copies each step block into one of two shared-
 // memory stages with one bulk copy, and the consumer records consumed[u] = c + 1
@@ -84,6 +84,11 @@ static_assert(OFF_JOB + 2 * sizeof(JobDesc) <= OFF_GL, "job area overflows");
 // the v tile's place (a producer has no v), so the q / k / g tiles are free
 // for the next job's load as soon as pass B is done.
 constexpr uint32_t P_GK = OFF_V;
+// The token range (cu[n], cu[n + 1]) of each sequence, by rank, read once
+// from cu and order so that a claim costs one atomic.
+constexpr uint32_t P_SEQ = kSmemUsed;
+constexpr uint32_t kSplitSmemBytes = kSmemBytes + kSplitMaxSeqs * 8;
+static_assert(P_SEQ % 8 == 0, "sequence table alignment");
 
 constexpr long long kPollTimeout = 1ll << 32;   // ~2 s of SM clock
 
@@ -324,11 +329,21 @@ __device__ __forceinline__ void producer(const Ctx& X, uint32_t tmem, int warp, 
         const long long total_jobs = (long long)U * ((maxlen + kC - 1) / kC);
         unsigned long long* counter = reinterpret_cast<unsigned long long*>(ws + kWsJobWord);
         const int32_t* order = ws + kWsHeaderBytes / sizeof(int32_t);
+        int2* seq_tab = reinterpret_cast<int2*>(sm + P_SEQ);
+        if (cu != nullptr) {
+            for (int r = lane; r < U / H; r += 32) {
+                const int n = order[r];
+                seq_tab[r] = make_int2(cu[n], cu[n + 1]);
+            }
+            __syncwarp();
+        }
         // Publishes job jc's slot once the compute group has written it.
         auto publish = [&](int jc) -> bool {
             if (!wait_bar(X, B_JOB_DONE, jc)) return false;
             const JobDesc& j = jd[jc & 1];
-            fence_acq_rel_gpu();
+            // The release store orders the slot's contents before the flag:
+            // the compute group's bulk stores completed and were fenced to
+            // the generic proxy before its CTA-scope hand-over (JOB_DONE).
             st_release_gpu(flags + (size_t)j.u * R + j.c % R, 2 * (j.c + 1) + (j.npass - 1));
             return true;
         };
@@ -352,9 +367,14 @@ __device__ __forceinline__ void producer(const Ctx& X, uint32_t tmem, int warp, 
                     c = (int)(j / U);
                     uu = (int)(j % U);
                     hh = uu % H;
-                    const int nn = (cu != nullptr) ? order[uu / H] : 0;
-                    bos = (cu != nullptr) ? cu[nn] : 0;
-                    eos = (cu != nullptr) ? cu[nn + 1] : total_tokens;
+                    if (cu != nullptr) {
+                        const int2 se = seq_tab[uu / H];
+                        bos = se.x;
+                        eos = se.y;
+                    } else {
+                        bos = 0;
+                        eos = total_tokens;
+                    }
                     if ((long long)c * kC < eos - bos) break;   // else: this unit has no chunk c
                 }
             }
@@ -484,10 +504,13 @@ __device__ __forceinline__ void producer(const Ctx& X, uint32_t tmem, int warp, 
                     bool free_slot = true;
                     if (p == 0) {
                         if (jc > 0) job_done(jc - 1, prev_npass);
+                        // No fence follows: the consumer records consumed[u]
+                        // only after its copy of chunk c - R has landed in
+                        // its shared memory, so the copy has read the slot
+                        // before the stores below are even issued.
                         if (seen < want)
                             free_slot = poll_flag(X, consumed + job.u,
                                                   [&](int32_t v) { return v >= want; }, &seen);
-                        fence_acq_rel_gpu();
                     }
                     // q, k, g and beta are read: the next job may be claimed
                     // and loaded.  (Only now: a producer that waits for a
@@ -599,12 +622,12 @@ cudaError_t launch_typed(const void* q, const void* k, const void* v, const floa
     static bool attr_set = false;   // benign race: every writer stores the same value
     if (!attr_set) {
         const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   (int)kSmemBytes);
+                                                   (int)kSplitSmemBytes);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
     int per_sm = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, kSmemBytes);
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, kSplitSmemBytes);
     if (e != cudaSuccess) return e;
     const int grid = plan.units + plan.producers;
     if (per_sm < 1 || grid > per_sm * device_sm_count()) return cudaErrorCooperativeLaunchTooLarge;
@@ -614,7 +637,7 @@ cudaError_t launch_typed(const void* q, const void* k, const void* v, const floa
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.dynamicSmemBytes = kSplitSmemBytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeCooperative;
