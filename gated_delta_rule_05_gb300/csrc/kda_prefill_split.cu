@@ -95,13 +95,16 @@ constexpr long long kPollTimeout = 1ll << 32;   // ~2 s of SM clock
 // Polls a global flag until pred(value) holds.  Returns false after about
 // kPollTimeout cycles (recording the timeout for the caller and the abort for
 // the other CTAs), or at once when another CTA has already given up.
-template <typename Pred>
+// ACQ = false polls with relaxed loads: an acquire load also waits for the
+// polling warp's own bulk copies still in flight, which the consumer's loader
+// must not do (see there).
+template <bool ACQ = true, typename Pred>
 __device__ __forceinline__ bool poll_flag(const Ctx& X, const int32_t* flag, Pred pred,
                                           int32_t* seen)
 {
     const long long t0 = clock64();
     for (int i = 0;; ++i) {
-        const int32_t v = ld_acquire_gpu(flag);
+        const int32_t v = ACQ ? ld_acquire_gpu(flag) : ld_relaxed_gpu(flag);
         if (pred(v)) {
             *seen = v;
             return true;
@@ -171,7 +174,15 @@ __device__ __forceinline__ void consumer(const Ctx& X, uint32_t tmem, int warp, 
             if (c + kVAhead < nch && !issue_v(c + kVAhead)) { ok = false; break; }
             const int slot = c % R;
             int32_t val = 0;
-            ok = poll_flag(X, full + slot, [&](int32_t v) { return (v >> 1) == c + 1; }, &val);
+            // Relaxed polls: an acquire load would also wait for this warp's
+            // copy of the previous chunk, still in flight, and so run the two
+            // stages one after the other; where copies are slow every step
+            // then took a whole copy.  The slot was complete before its flag
+            // was stored (the producer's bulk stores had completed and been
+            // fenced before the release store), the copy below is issued
+            // only after the flag has been read and reads global memory at
+            // L2, and the proxy fence orders the two reads.
+            ok = poll_flag<false>(X, full + slot, [&](int32_t v) { return (v >> 1) == c + 1; }, &val);
             if (!ok) break;
             fence_proxy_async_global();        // the bulk copies below read what the producer wrote
             const int npass = (val & 1) + 1;
@@ -217,7 +228,9 @@ __device__ __forceinline__ void consumer(const Ctx& X, uint32_t tmem, int warp, 
             const int vb = d.chunk & (kVBufs - 1);
             // The compute group saw this block land: the ring slot is free
             // once the chunk's last block is here.
-            if (d.last_pass && lane == 0) st_relaxed_gpu(consumed, d.chunk + 1);
+            // (A reduction rather than a store: it is performed at L2 at
+            // once, so waiting producers see the free slot promptly.)
+            if (d.last_pass && lane == 0) red_max_relaxed_gpu(consumed, d.chunk + 1);
             mma_back_c(tmem, blk + BLK_WT, blk + BLK_T16, smem_u32(sm + C_V0 + vb * 16384));
             mma_commit(&X.bar[B_MMA_C]);
             if (d.last_pass) mma_commit(&X.bar[B_SV_EMPTY0 + vb]);

@@ -210,6 +210,13 @@ __device__ __forceinline__ void st_relaxed_gpu(int32_t* p, int32_t v)
     asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+// Raises *p to at least v with a reduction performed at L2 (no value
+// returned, no fence): the new value becomes visible to pollers promptly.
+__device__ __forceinline__ void red_max_relaxed_gpu(int32_t* p, int32_t v)
+{
+    asm volatile("red.relaxed.gpu.global.max.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ void fence_acq_rel_gpu()
 {
     asm volatile("fence.acq_rel.gpu;" ::: "memory");
