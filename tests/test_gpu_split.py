@@ -77,6 +77,11 @@ CASES = {
     "varlen_empty_ragged": ([0, 300, 0, 130, 64, 1, 65], 2),
     "one_unit_long": ([5000], 1),
     "many_chunks_few_units": ([20000], 4),
+    # more sequences than a warp's lanes: the producers' table of sequence
+    # ranges is filled in two strides; 76 units is the split path's maximum on
+    # 152 SMs (half of them)
+    "many_seqs": ([(37 * i) % 257 for i in range(40)], 1),
+    "max_units": ([(53 * i + 11) % 193 for i in range(76)], 1),
 }
 
 
