@@ -65,9 +65,9 @@ typedef enum {
  * heads.  The workspace always holds the varlen work list (sequences ordered
  * longest first, counters, an error word).  When d_k = d_v = 128 and the
  * num_seqs x H (sequence, head) units fill at most half of the current
- * device's SMs, the value also covers the operand ring of the producer /
- * consumer prefill kernel (tens of MB at most; the size depends on the SM
- * count).  Returns 0 when num_seqs < 1. */
+ * device's SMs (and num_seqs <= 128), the value also covers the operand ring
+ * of the producer / consumer prefill kernel (tens of MB at most; the size
+ * depends on the SM count).  Returns 0 when num_seqs < 1. */
 size_t kda_prefill_workspace_bytes(int32_t num_seqs, int32_t H, int32_t d_k,
                                    int32_t d_v);
 
