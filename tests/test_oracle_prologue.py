@@ -40,3 +40,18 @@ def test_qk_normalisation():
     qh2, kh2, _ = oracle.gate_prologue(3.0 * q, 0.5 * k, z, A, 0.125)
     np.testing.assert_allclose(qh2, qh, rtol=1e-14)
     np.testing.assert_allclose(kh2, kh, rtol=1e-14)
+
+
+def test_gate_value_with_nonzero_A():
+    # e^A z = 1 at A = ln 2, z = 1/2, so g = -5 sigmoid(1); the slip e^{-A}
+    # would give e^{-A} z = 1/4 instead, and a missing exponential A z = ln2/2.
+    H, d = 1, 4
+    A = np.full((H, d), np.log(2.0))
+    z = np.full((1, H, d), 0.5)
+    _, _, g = oracle.gate_prologue(np.ones((1, H, d)), np.ones((1, H, d)), z, A, 1.0)
+    np.testing.assert_allclose(g, -5.0 / (1.0 + np.exp(-1.0)), rtol=1e-15)
+    # A = ln 4, z = -1/8: e^A z = -1/2
+    A = np.full((H, d), np.log(4.0))
+    z = np.full((1, H, d), -0.125)
+    _, _, g = oracle.gate_prologue(np.ones((1, H, d)), np.ones((1, H, d)), z, A, 1.0)
+    np.testing.assert_allclose(g, -5.0 / (1.0 + np.exp(0.5)), rtol=1e-15)
