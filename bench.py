@@ -10,10 +10,15 @@ One step is one pass of the hot path over one batch:
   * decode   -- kda_decode_step over decode_1024x32 (1024 sequences x 32
                 heads, d=128, 2 GiB fp32 state updated in place); reported in
                 the ``decode`` object as achieved state GB/s.
-Both are timed with CUDA events on the launching stream, W untimed warm-up
+Two more prefill workloads are reported beside them: ``varlen`` (varlen16_h32,
+16 packed sequences with S0 in and S_final out) and ``short``
+(prefill_h16_t4096, one 4096-token prompt of 16 heads).
+Each is timed with CUDA events on the launching stream, W untimed warm-up
 steps first, each timed region bracketed by a barrier and a device
 synchronisation, max over ranks.  Inputs are far larger than L2 (51.7 GB per
-prefill step, 2 GiB of state per decode step), so no L2 flush is needed.
+prefill step, 2 GiB of state per decode step) except for ``short`` (102 MB),
+which flushes L2 before every timed launch.  After each prefill section the
+workspace's device status words are read; a wait that gave up voids the run.
 
 Under torchrun each rank processes its own batch (independent sequences, no
 data-path collective: weak scaling); the process group is used only for the
@@ -278,6 +283,20 @@ def run_reference(args):
 # --------------------------------------------------------------------------
 # the CUDA path
 # --------------------------------------------------------------------------
+class DeviceWaitGaveUp(RuntimeError):
+    """A timed launch reported a device-side wait that gave up: its outputs
+    are incomplete and its time is not a measurement."""
+
+
+def check_status_words(ws, what):
+    """The prefill workspace's device-side status words after a timed section
+    (the caller zeroes the workspace before it): word 2 bit 1 = a wait gave
+    up, word 6 = the producer / consumer kernel aborted, word 1 = invalid
+    cu_seqlens.  Any of them set voids the section's numbers."""
+    words = ws[:28].view(dtype=__import__("torch").int32).cpu().tolist()
+    if words[2] & 2 or words[6] != 0 or words[1] != 0:
+        raise DeviceWaitGaveUp("%s: device status words timeout=%d abort=%d cu_error=%d; "
+                               "refusing to report a time" % (what, words[2], words[6], words[1]))
 # The prefill kernel that dominates the timed call, and the sources that
 # define it: the producer / consumer kernel when the workspace kda_prefill
 # asks for includes its operand ring (few (sequence, head) units), else the
@@ -325,9 +344,11 @@ def run_kda(args):
         line["decode"] = bench_decode(args, kda, torch, synth, peaks, stream, dev, rank, world, smi_id)
     if args.only in ("all", "varlen"):
         line["varlen"] = bench_varlen(args, kda, torch, synth, peaks, stream, dev, rank, world, smi_id)
+    if args.only in ("all", "short"):
+        line["short"] = bench_short(args, kda, torch, synth, peaks, stream, dev, rank, world, smi_id)
     if rank == 0:
-        if "value" not in line:        # decode or varlen only: that section leads the line
-            d = line["decode"] if "decode" in line else line["varlen"]
+        if "value" not in line:        # one section only: that section leads the line
+            d = next(line[k] for k in ("decode", "varlen", "short") if k in line)
             line.update({"metric": METRIC, "value": d["value"], "unit": d["unit"], "n_gpus": world,
                          "steps": args.steps, "warmup": args.warmup,
                          "ms_per_step": d["ms_per_step"], "higher_is_better": True,
@@ -337,9 +358,8 @@ def run_kda(args):
                          "gpu_launches": d["gpu_launches"], "cpu_baseline": None,
                          "e2e": None})
         else:
-            line["gpu_launches"] = line.get("gpu_launches", 0) + \
-                line.get("decode", {}).get("gpu_launches", 0) + \
-                line.get("varlen", {}).get("gpu_launches", 0)
+            line["gpu_launches"] = line.get("gpu_launches", 0) + sum(
+                line.get(k, {}).get("gpu_launches", 0) for k in ("decode", "varlen", "short"))
         if args.only == "all" and world == 1 and not args.no_cpu:
             line["cpu_baseline"] = cpu_baseline()   # rank 0 at N=1 only
         print(json.dumps(line), flush=True)
@@ -358,12 +378,14 @@ def bench_prefill(args, kda, torch, synth, peaks, stream, dev, rank, world, smi_
                          seed=rank_seed(wp.seed, rank), device=dev)
     T, H, d = inp.q.shape
     o = torch.empty((T, H, d), dtype=inp.q.dtype, device=dev)
-    ws = torch.empty(kda.kda_prefill_workspace_bytes(1, H, d, d), dtype=torch.uint8, device=dev)
+    S_final = torch.empty((1, H, d, d), dtype=torch.float32, device=dev)
+    # zeroed: the timeout word is never cleared by the library
+    ws = torch.zeros(kda.kda_prefill_workspace_bytes(1, H, d, d), dtype=torch.uint8, device=dev)
     kernel = prefill_kernel_name(ws.numel(), 1)
 
     def prefill():
         kda.kda_prefill(inp.q, inp.k, inp.v, inp.log_alpha, inp.beta, S0=None,
-                        cu_seqlens=inp.cu_seqlens, o=o, want_state=False,
+                        cu_seqlens=inp.cu_seqlens, o=o, S_final=S_final,
                         workspace=ws, stream=stream)
 
     for _ in range(args.warmup):
@@ -382,13 +404,14 @@ def bench_prefill(args, kda, torch, synth, peaks, stream, dev, rank, world, smi_
         torch.cuda.synchronize(dev)
         t_wall = time.perf_counter() - t_wall
     barrier(world)
+    check_status_words(ws, workload)
     prefill_ms = sum(s.elapsed_time(e) for s, e in ev)
     prefill_ms_max = max_over_ranks(prefill_ms, world, dev)
     ms_per_step = prefill_ms_max / args.steps
     tokens_all = T * world * args.steps
     value = tokens_all / (prefill_ms_max / 1e3)
     launch_ms = prefill_ms / args.steps          # this rank, per launch
-    alg_bytes = T * H * BYTES_PER_TOKEN_HEAD
+    alg_bytes = T * H * BYTES_PER_TOKEN_HEAD + H * state_bytes(d)     # + the S_final write
     alg_flops = T * H * FLOPS_PER_TOKEN_HEAD
     achieved = alg_bytes / (launch_ms / 1e3) / 1e9
     traffic = committed_traffic(workload + "/" + kernel, PREFILL_KERNELS[kernel])
@@ -405,6 +428,7 @@ def bench_prefill(args, kda, torch, synth, peaks, stream, dev, rank, world, smi_
         "dtype": "bf16", "data": "synthetic",
         "config": {"workload": workload, "num_seqs": 1, "seq_len": T, "H": H,
                    "d_k": d, "d_v": d, "io_dtype": "bf16", "state_dtype": "fp32",
+                   "S0": None, "S_final": "written",
                    "tokens_per_step_per_gpu": T, "parallelism": "dp%d" % world,
                    "l2": "inputs larger than L2 (%.1f GB per step)" % (alg_bytes / 1e9)},
         "roofline": roofline,
@@ -482,7 +506,7 @@ def bench_varlen(args, kda, torch, synth, peaks, stream, dev, rank, world, smi_i
     T, H, d = vin.q.shape
     ov = torch.empty_like(vin.v)
     Sf = torch.empty_like(vin.S0)
-    ws = torch.empty(kda.kda_prefill_workspace_bytes(N, H, d, d), dtype=torch.uint8, device=dev)
+    ws = torch.zeros(kda.kda_prefill_workspace_bytes(N, H, d, d), dtype=torch.uint8, device=dev)
     kernel = prefill_kernel_name(ws.numel(), N)
 
     def run():
@@ -503,6 +527,7 @@ def bench_varlen(args, kda, torch, synth, peaks, stream, dev, rank, world, smi_i
             e.record(stream)
         torch.cuda.synchronize(dev)
     barrier(world)
+    check_status_words(ws, name)
     ms = sum(s.elapsed_time(e) for s, e in ev)
     ms_max = max_over_ranks(ms, world, dev)
     alg_bytes = T * H * BYTES_PER_TOKEN_HEAD + 2 * N * H * d * d * 4   # + S0 read, S_final write
@@ -518,6 +543,67 @@ def bench_varlen(args, kda, torch, synth, peaks, stream, dev, rank, world, smi_i
                      "algorithmic_bytes_per_launch": alg_bytes},
         # per call: the work-list kernel + the tensor-core kernel
         "gpu_launches": 2 * args.steps,
+        "clocks": clk.summary(),
+    }
+
+
+SHORT_WORKLOAD = 2            # prefill_h16_t4096
+L2_FLUSH_BYTES = 512 << 20    # well above the 129 MB L2
+
+
+def bench_short(args, kda, torch, synth, peaks, stream, dev, rank, world, smi_id):
+    """prefill_h16_t4096: one 4096-token sequence of 16 heads (102 MB of
+    inputs and outputs, less than L2), S_final returned.  16 units: the
+    producer / consumer kernel with a 64-chunk chain per unit.  L2 is flushed
+    (a 512 MB write) before every timed launch, outside its events."""
+    ws_ = synth.WORKLOADS[SHORT_WORKLOAD]
+    sin = synth.generate(synth.draw_lengths(ws_), ws_.H, ws_.d, ws_.d, dtype=ws_.dtype,
+                         gate=ws_.gate, q_scale=ws_.q_scale, s0_std=ws_.s0_std,
+                         seed=rank_seed(ws_.seed, rank), device=dev)
+    T, H, d = sin.q.shape
+    o = torch.empty_like(sin.v)
+    Sf = torch.empty((1, H, d, d), dtype=torch.float32, device=dev)
+    ws = torch.zeros(kda.kda_prefill_workspace_bytes(1, H, d, d), dtype=torch.uint8, device=dev)
+    kernel = prefill_kernel_name(ws.numel(), 1)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def run():
+        kda.kda_prefill(sin.q, sin.k, sin.v, sin.log_alpha, sin.beta, S0=None,
+                        cu_seqlens=None, o=o, S_final=Sf, workspace=ws, stream=stream)
+
+    steps = max(args.steps, 20)
+    for _ in range(max(args.warmup, 3)):
+        run()
+    torch.cuda.synchronize(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(smi_id) as clk, torch.cuda.stream(stream):
+        for s, e in ev:
+            flush.fill_(1)
+            s.record(stream)
+            run()
+            e.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier(world)
+    check_status_words(ws, ws_.name)
+    times = sorted(s.elapsed_time(e) for s, e in ev)
+    ms = sum(times)
+    ms_max = max_over_ranks(ms, world, dev)
+    alg_bytes = T * H * BYTES_PER_TOKEN_HEAD + H * state_bytes(d)       # + the S_final write
+    achieved = alg_bytes / (ms / steps / 1e3) / 1e9
+    return {
+        "value": T * world * steps / (ms_max / 1e3), "unit": "tokens/s",
+        "ms_per_step": ms_max / steps, "ms_median": times[len(times) // 2],
+        "workload": ws_.name, "tokens_per_step": T * world, "steps": steps,
+        "l2": "flushed before each timed launch (%d MB write)" % (L2_FLUSH_BYTES >> 20),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                     "traffic": None, "peak_source": peaks["source"], "kernel": kernel,
+                     "algorithmic_bytes_per_launch": alg_bytes},
+        # per call: the work-list kernel + the tensor-core kernel
+        "gpu_launches": 2 * steps,
         "clocks": clk.summary(),
     }
 
@@ -645,7 +731,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["kda", "reference"], default="kda")
-    ap.add_argument("--only", choices=["all", "prefill", "decode", "varlen"], default="all",
+    ap.add_argument("--only", choices=["all", "prefill", "decode", "varlen", "short"],
+                    default="all",
                     help="time only one part (profiling runs)")
     ap.add_argument("--tokens", type=int, default=0,
                     help="prefill length override (profiling runs on a smaller case)")

@@ -17,7 +17,15 @@
 //     call on each device, with that device current, looks its address up
 //     with cudaGetSymbolAddress (which may load the library's device code),
 //     so make that first call before any stream capture starts.  Later calls
-//     on the same device reuse the address.
+//     on the same device reuse the address while the device's current
+//     context is the one it was looked up in; a new context (after
+//     cudaDeviceReset, for example) has its own copy of the array, and its
+//     address is looked up again.
+//   * The status words kda_prefill leaves in its workspace (an invalid
+//     cu_seqlens, a wait that gave up) stay in this private array, where
+//     the caller cannot read them.
+//   * The array has room for the work list only, so the producer / consumer
+//     kernel (whose operand ring needs tens of MB) is never selected.
 //   * Every call on a device shares the same array.  Calls that may overlap
 //     on the GPU (on different streams, or from different host threads
 //     without ordering) race on it and must not be issued that way.
@@ -26,6 +34,8 @@
 //     work counter and error word before any kernel reads them, and a call
 //     without cu_seqlens reads none of it.
 //   * Nothing here calls cudaMalloc, cudaFree or any allocating routine.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "kda_internal.cuh"
@@ -40,19 +50,48 @@ constexpr int kMaxDevices = 64;
 __device__ __align__(256) unsigned char g_prefill_scratch[kNoAllocScratchBytes];
 
 std::mutex g_mu;
+// Per device: the context the address was looked up in, and the address.
+CUcontext g_scratch_ctx[kMaxDevices] = {};
 void* g_scratch_addr[kMaxDevices] = {};
 
-// Device address of the scratch array on the current device; nullptr if the
-// lookup fails.
+// The driver's cuCtxGetCurrent, looked up once through the runtime (the
+// library does not link the driver library itself).
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+CtxGetCurrentFn ctx_get_current_fn()
+{
+    static CtxGetCurrentFn fn = nullptr;
+    static bool looked = false;
+    if (!looked) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<CtxGetCurrentFn>(p);
+        looked = true;
+    }
+    return fn;
+}
+
+// Device address of the scratch array in the current device's current
+// context; nullptr if the lookup fails.
 void* scratch_on_current_device()
 {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
     std::lock_guard<std::mutex> lock(g_mu);
-    if (g_scratch_addr[dev] == nullptr) {
+    CtxGetCurrentFn get_ctx = ctx_get_current_fn();
+    if (get_ctx == nullptr) return nullptr;
+    // Before the runtime's first use of the device no context is current yet
+    // (ctx stays null); cudaGetSymbolAddress then makes it current.
+    CUcontext ctx = nullptr;
+    if (get_ctx(&ctx) != CUDA_SUCCESS) return nullptr;
+    if (ctx == nullptr || g_scratch_addr[dev] == nullptr || g_scratch_ctx[dev] != ctx) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_prefill_scratch) != cudaSuccess) return nullptr;
+        if (get_ctx(&ctx) != CUDA_SUCCESS || ctx == nullptr) return nullptr;
         g_scratch_addr[dev] = p;
+        g_scratch_ctx[dev] = ctx;
     }
     return g_scratch_addr[dev];
 }

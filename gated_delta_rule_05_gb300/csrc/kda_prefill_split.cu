@@ -25,10 +25,14 @@
 // whose decay span needs two passes fills two step blocks.  The producer's
 // data-movement warp then publishes the slot with a release store of
 // full[u][slot] = 2 (c + 1) + (passes - 1).  The consumer's loader polls that
-// word with acquire loads, copies each step block into one of two shared-
-// memory stages with one bulk copy, and the consumer records consumed[u] = c + 1
-// once the copy has landed.  A producer writes a slot only when consumed[u]
-// shows that the chunk R places earlier has left it.
+// word with relaxed loads and, once it shows the chunk, issues an acquire
+// fence (the relaxed load and the fence form an acquire pattern that
+// synchronises with the release store) and a proxy fence, then copies each
+// step block into one of two shared-memory stages with one bulk copy.  The
+// consumer raises consumed[u] to c + 1 with a relaxed reduction once the copy
+// has landed (see the MMA warp for why not a release); a producer writes a
+// slot only after an acquire of consumed[u] shows that the chunk R places
+// earlier has left it.
 //
 // Progress.  Jobs are claimed in order and every job depends only on jobs of
 // earlier chunks, and a producer publishes a job before it waits for the slot
@@ -39,6 +43,13 @@
 // before the launch), every other CTA polling a global flag sees the abort and
 // stops, and each CTA waits for its own copies in flight and frees its tensor
 // memory before it exits.
+//
+// Test hook.  With KDA_TEST_STARVE_CONSUMERS set in the environment, the
+// launch runs the abort path on purpose: the producers exit at once without
+// publishing anything.  The consumers' waits then run out after their usual
+// limit (about two seconds), the timeout bit and the abort word are set,
+// every CTA drains and exits, and o and S_final are not written.  It exists
+// for the test of that path only.
 #include <cudaTypedefs.h>
 #include <stdio.h>
 #include <stdlib.h>
@@ -90,10 +101,8 @@ constexpr uint32_t P_SEQ = kSmemUsed;
 constexpr uint32_t kSplitSmemBytes = kSmemBytes + kSplitMaxSeqs * 8;
 static_assert(P_SEQ % 8 == 0, "sequence table alignment");
 
-constexpr long long kPollTimeout = 1ll << 32;   // ~2 s of SM clock
-
 // Polls a global flag until pred(value) holds.  Returns false after about
-// kPollTimeout cycles (recording the timeout for the caller and the abort for
+// kWaitLimit cycles (recording the timeout for the caller and the abort for
 // the other CTAs), or at once when another CTA has already given up.
 // ACQ = false polls with relaxed loads: an acquire load also waits for the
 // polling warp's own bulk copies still in flight, which the consumer's loader
@@ -111,7 +120,7 @@ __device__ __forceinline__ bool poll_flag(const Ctx& X, const int32_t* flag, Pre
         }
         if ((i & 31) == 31) {
             if (ld_relaxed_gpu(X.ws_abort) != 0) return false;
-            if (clock64() - t0 > kPollTimeout) {
+            if (clock64() - t0 > kWaitLimit) {
                 atomicOr(X.ws_err, 2);
                 atomicExch(X.ws_abort, 1);
                 return false;
@@ -179,11 +188,13 @@ __device__ __forceinline__ void consumer(const Ctx& X, uint32_t tmem, int warp, 
             // stages one after the other; where copies are slow every step
             // then took a whole copy.  The slot was complete before its flag
             // was stored (the producer's bulk stores had completed and been
-            // fenced before the release store), the copy below is issued
-            // only after the flag has been read and reads global memory at
-            // L2, and the proxy fence orders the two reads.
+            // fenced before the release store).  The acquire fence after the
+            // poll that saw the flag makes the poll an acquire: the
+            // producer's writes happen before this thread's later accesses,
+            // and the proxy fence extends that order to the bulk copies below.
             ok = poll_flag<false>(X, full + slot, [&](int32_t v) { return (v >> 1) == c + 1; }, &val);
             if (!ok) break;
+            fence_acquire_gpu();
             fence_proxy_async_global();        // the bulk copies below read what the producer wrote
             const int npass = (val & 1) + 1;
             const long long t0 = bos + (long long)c * kC;
@@ -227,9 +238,15 @@ __device__ __forceinline__ void consumer(const Ctx& X, uint32_t tmem, int warp, 
             const uint32_t blk = smem_u32(sm + (step & 1) * kStage);
             const int vb = d.chunk & (kVBufs - 1);
             // The compute group saw this block land: the ring slot is free
-            // once the chunk's last block is here.
-            // (A reduction rather than a store: it is performed at L2 at
-            // once, so waiting producers see the free slot promptly.)
+            // once the chunk's last block is here.  (A reduction rather than
+            // a store: it is performed at L2 at once, so waiting producers
+            // see the free slot promptly.  Relaxed: the bulk copies that read
+            // the slot have completed before this point, so nothing the
+            // producer writes afterwards can reach them.  A release form,
+            // which the PTX memory model would also order formally, measured
+            // slower at 1M tokens x 32 heads: 27 % here, where it waits for
+            // the warp's products in flight; 46 % from a compute thread; 6 %
+            // from an eleventh warp that did nothing else.)
             if (d.last_pass && lane == 0) red_max_relaxed_gpu(consumed, d.chunk + 1);
             mma_back_c(tmem, blk + BLK_WT, blk + BLK_T16, smem_u32(sm + C_V0 + vb * 16384));
             mma_commit(&X.bar[B_MMA_C]);
@@ -517,13 +534,17 @@ __device__ __forceinline__ void producer(const Ctx& X, uint32_t tmem, int warp, 
                     bool free_slot = true;
                     if (p == 0) {
                         if (jc > 0) job_done(jc - 1, prev_npass);
-                        // No fence follows: the consumer records consumed[u]
-                        // only after its copy of chunk c - R has landed in
-                        // its shared memory, so the copy has read the slot
-                        // before the stores below are even issued.
+                        // The consumer raises consumed[u] only after its
+                        // copy of chunk c - R has landed in its shared
+                        // memory.  The acquire fence turns the relaxed first
+                        // look into an acquire (the poll's loads already
+                        // are), and the proxy fence orders the bulk stores
+                        // below after it.
                         if (seen < want)
                             free_slot = poll_flag(X, consumed + job.u,
                                                   [&](int32_t v) { return v >= want; }, &seen);
+                        fence_acquire_gpu();
+                        fence_proxy_async_global();
                     }
                     // q, k, g and beta are read: the next job may be claimed
                     // and loaded.  (Only now: a producer that waits for a
@@ -570,7 +591,8 @@ prefill_split_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                      const __grid_constant__ CUtensorMap tm_o, const float* __restrict__ beta,
                      const float* S0, const int32_t* __restrict__ cu, int32_t* ws,
                      long long total_tokens, int H, TO* __restrict__ o, float* S_final, int U, int R,
-                     int32_t* flags, uint8_t* ring, const SnapArgs snap, const GateArgs gate)
+                     int32_t* flags, uint8_t* ring, const SnapArgs snap, const GateArgs gate,
+                     int test_starve)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -603,7 +625,7 @@ prefill_split_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     if ((int)blockIdx.x < U)
         consumer<TO>(X, tmem, warp, lane, &tm_v, &tm_o, S0, cu, ws, total_tokens, H, o, S_final, U,
                      R, flags, ring, snap);
-    else
+    else if (!test_starve)
         producer<TO, FUSED>(X, tmem, warp, lane, &tm_q, &tm_k, &tm_g, beta, cu, ws, total_tokens, H, U,
                         R, flags, ring, gate);
 
@@ -657,9 +679,10 @@ cudaError_t launch_typed(const void* q, const void* k, const void* v, const floa
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    const int test_starve = getenv("KDA_TEST_STARVE_CONSUMERS") != nullptr ? 1 : 0;
     e = cudaLaunchKernelEx(&cfg, kern, mq, mk, mg, mv, mo, beta, S0, cu, ws, (long long)T, (int)H,
                            static_cast<TO*>(o), S_final, (int)plan.units, (int)plan.ring, flags,
-                           ring, snap, gate);
+                           ring, snap, gate, test_starve);
     if (e != cudaSuccess && debug_enabled())
         fprintf(stderr, "kda: prefill_split launch failed: %s\n", cudaGetErrorString(e));
     return e;

@@ -222,6 +222,15 @@ __device__ __forceinline__ void fence_acq_rel_gpu()
     asm volatile("fence.acq_rel.gpu;" ::: "memory");
 }
 
+// After a relaxed load that observed a value written by a release (store or
+// reduction) in another CTA: together they form an acquire pattern, so this
+// thread's later accesses are ordered after everything the releasing thread
+// did before its release.
+__device__ __forceinline__ void fence_acquire_gpu()
+{
+    asm volatile("fence.acquire.gpu;" ::: "memory");
+}
+
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map)
 {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");

@@ -32,6 +32,13 @@
  *    L2-normalised and q pre-scaled by the caller (the op uses them as given);
  *    beta is any finite value (beta up to 2 gives a reflection, "Kimi 모델
  *    분석", rlaope.github.io, section "반사가 계층을 바꿈"); inputs finite.
+ *    On the tensor-core path (bf16 q/k/v with d_k = d_v = 128, see
+ *    kda_prefill's Paths) v, the states (S0 and every state the recurrence
+ *    passes through) and the chunk products formed from them enter the
+ *    tensor cores as fp16, so |v| and every state entry must stay below
+ *    65504, the largest finite fp16 value; beyond it the results are not
+ *    finite.  The fp32 CUDA-core path has no such limit: a caller whose
+ *    values may exceed it passes fp32 inputs (KDA_FP32).
  *  - Supported shapes: every dtype code with d_k = d_v in {16, 32, 64, 128}.
  *    Anything else returns KDA_ERR_UNSUPPORTED.
  */
@@ -307,11 +314,24 @@ kda_status_t kda_state_gather(const float *states, const float *S_in,
  * returns KDA_ERR_WORKSPACE.  The first call on each device, with that device
  * current, looks the array's device address up (cudaGetSymbolAddress, which
  * may load the library's device code), so make that first call before any
- * stream capture.  All calls on a device share the array: calls that may
- * overlap on the GPU race on it and must be ordered by the caller.  Nothing
- * is allocated and nothing in the array needs clearing between calls.
- * KDA_ERR_CUDA is returned if the device or the array's address cannot be
- * determined. */
+ * stream capture; the address is looked up again only when the device's
+ * current context changes (after cudaDeviceReset, for example).  All calls on
+ * a device share the array: calls that may overlap on the GPU race on it and
+ * must be ordered by the caller.  Nothing is allocated and nothing in the
+ * array needs clearing between calls.  KDA_ERR_CUDA is returned if the
+ * device or the array's address cannot be determined.
+ *
+ * What differs from kda_prefill:
+ *  - The device-side status words (invalid cu_seqlens, a wait that gave up)
+ *    live in the private array and cannot be read by the caller.  An invalid
+ *    cu_seqlens therefore still returns KDA_OK, with o and S_final not
+ *    written; a caller that cannot vouch for its cu_seqlens validates it
+ *    before the call, or calls kda_prefill.
+ *  - The array has room for the work list only, never for the operand ring
+ *    of the producer / consumer kernel, so every call takes the one-CTA-per-
+ *    (sequence, head) kernel.  The results are the same, but a batch with few
+ *    units (one long sequence of 32 heads, say) keeps only that many SMs
+ *    busy: several times slower than kda_prefill with a full workspace. */
 kda_status_t kda_prefill_noalloc(const void *q, const void *k, const void *v,
                                  const float *log_alpha, const float *beta,
                                  const float *S0, const int32_t *cu_seqlens,

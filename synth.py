@@ -15,7 +15,7 @@ Workloads (named by what they are):
   decode_1024x32         1024 seqs x H=32, one token each, d=128, bf16,
                          state S ~ N(0, 0.02^2) fp32
 
-Distributions (from the pages' description of KDA inputs):
+Distributions (the pages describe KDA's inputs; these are the synthetic stand-ins):
   q ~ N(0,1), scaled by 1/sqrt(d_k) for the d=128 workloads;
   k ~ N(0,1), L2-normalised per (token, head) in fp32 before any cast;
   v ~ N(0,1);

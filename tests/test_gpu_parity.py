@@ -70,10 +70,23 @@ def test_varlen16_h32_sampled_columns(kda):
     check_prefill(kda, inp, "bf16", cols=[0, 17, 38, 63, 64, 90, 111, 127])
 
 
+def test_varlen16_h32_sampled_columns_fp32_output(kda):
+    # bf16 inputs, fp32 output: the plain bound on the varlen workload.
+    inp = synth.workload_inputs(3, device="cuda")
+    check_prefill(kda, inp, "bf16", cols=[3, 29, 64, 100, 127], o_dtype=torch.float32)
+
+
 def test_prefill_h32_t1m_sampled(kda):
     inp = synth.workload_inputs(4, device="cuda")
     check_prefill(kda, inp, "bf16", heads=[0, 31], cols=[0, 5, 64, 127],
                   seg=1 << 17)
+
+
+def test_prefill_h32_t1m_sampled_fp32_output(kda):
+    # The plain bound (no output rounding) on the 1M-token workload.
+    inp = synth.workload_inputs(4, device="cuda")
+    check_prefill(kda, inp, "bf16", heads=[7, 20], cols=[1, 66, 126],
+                  seg=1 << 17, o_dtype=torch.float32)
 
 
 def test_decode_1024x32(kda):
@@ -135,6 +148,18 @@ def test_beta_two(kda):
     inp = synth.generate([200], 2, 64, 64, dtype="fp32", s0_std=0.1, seed=12)
     inp.beta.fill_(2.0)
     check_prefill(kda, inp, "fp32")
+
+
+@pytest.mark.parametrize("gates", ["alpha_one", "realistic"])
+def test_beta_two_tensor_cores(kda, gates):
+    # beta = 2 on the tensor-core path (bf16, d = 128) with 180 units, more
+    # than half the SMs: the single-CTA kernel.
+    shift = 0.0 if gates == "alpha_one" else None
+    inp = synth.generate([130, 64, 255] * 3, 20, 128, 128, dtype="bf16", s0_std=0.05,
+                         seed=16 + len(gates), gate_shift=shift)
+    inp.beta.fill_(2.0)
+    check_prefill(kda, inp, "bf16")
+    check_prefill(kda, inp, "bf16", o_dtype=torch.float32)
 
 
 # --- chaining, in-place resume, decode == prefill ---------------------------

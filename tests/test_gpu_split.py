@@ -123,6 +123,20 @@ def test_split_all_wide_fp32_output(kda):
     check(kda, inp, o_dtype=torch.float32)
 
 
+@pytest.mark.parametrize("gates", ["alpha_one", "realistic"])
+def test_split_beta_two(kda, gates):
+    # beta = 2 on both tensor-core kernels ("Kimi 모델 분석", section "반사가
+    # 계층을 바꿈": with alpha = 1 and a unit key the step is the reflection
+    # I - 2 k k^T).  T = (I + A)^{-1} Diag(beta) and the fp16 operands grow
+    # with beta; nothing in the kernels may assume beta <= 1.
+    shift = 0.0 if gates == "alpha_one" else None
+    inp = synth.generate([777, 64, 200], 2, 128, 128, dtype="bf16", s0_std=0.05,
+                         seed=620 + len(gates), gate_shift=shift)
+    inp.beta.fill_(2.0)
+    check(kda, inp)
+    check(kda, inp, o_dtype=torch.float32)
+
+
 def test_split_back_to_back_reuses_workspace(kda):
     # Two calls on one workspace: the work-list kernel clears the hand-over
     # flags and counters in between.
@@ -157,3 +171,39 @@ def test_split_ignores_workspace_contents(kda):
     torch.cuda.synchronize()
     assert torch.equal(o, o1)
     assert torch.equal(S, S1)
+
+
+def test_split_abort_path(kda, monkeypatch):
+    # The bounded waits' abort path, run on purpose through the library's test
+    # hook: the producers exit without publishing anything and every wait
+    # gives up after about 2^20 cycles.  The call must return (every CTA
+    # exits), with the timeout bit and the abort word set and o untouched; the
+    # next normal call on the same workspace must be correct.  Nothing here
+    # traps or waits without a bound.
+    inp = synth.generate([700, 300], 2, 128, 128, dtype="bf16", s0_std=0.05, seed=630)
+    d = inp.to("cuda")
+    need = kda.kda_prefill_workspace_bytes(2, 2, 128, 128)
+    assert need > base_workspace_bytes(2)
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    o = torch.full_like(d.v, 5.0)
+    S = torch.full_like(d.S0, 5.0)
+    monkeypatch.setenv("KDA_TEST_STARVE_CONSUMERS", "1")
+    kda.kda_prefill(d.q, d.k, d.v, d.log_alpha, d.beta, S0=d.S0, cu_seqlens=d.cu_seqlens,
+                    o=o, S_final=S, workspace=ws)
+    torch.cuda.synchronize()
+    monkeypatch.delenv("KDA_TEST_STARVE_CONSUMERS")
+    words = ws[:28].view(torch.int32).cpu().tolist()
+    assert words[2] & 2, "the timeout bit must be set"
+    assert words[6] != 0, "the abort word must be set"
+    assert torch.all(o == 5.0) and torch.all(S == 5.0), "an aborted launch writes no result"
+    # the next call: the work-list kernel clears the flags and the abort word
+    # (the timeout word is the caller's to clear)
+    ws[8:12].zero_()
+    o2, S2 = kda.kda_prefill(d.q, d.k, d.v, d.log_alpha, d.beta, S0=d.S0,
+                             cu_seqlens=d.cu_seqlens, workspace=ws)
+    torch.cuda.synchronize()
+    words = ws[:28].view(torch.int32).cpu().tolist()
+    assert words[2] == 0 and words[6] == 0
+    o_ref, S_ref = oracle_prefill(inp)
+    compare_out(o2, o_ref, TOL["bf16"], "o after the aborted call")
+    assert_close(to64(S2), S_ref, TOL["bf16"], "S_final after the aborted call")
