@@ -566,29 +566,40 @@ def bench_short(args, kda, torch, synth, peaks, stream, dev, rank, world, smi_id
     ws = torch.zeros(kda.kda_prefill_workspace_bytes(1, H, d, d), dtype=torch.uint8, device=dev)
     kernel = prefill_kernel_name(ws.numel(), 1)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    ws_seg = torch.zeros(kda.kda_prefill_segmented_workspace_bytes(T, H, d, d, 0),
+                         dtype=torch.uint8, device=dev)
 
     def run():
         kda.kda_prefill(sin.q, sin.k, sin.v, sin.log_alpha, sin.beta, S0=None,
                         cu_seqlens=None, o=o, S_final=Sf, workspace=ws, stream=stream)
 
+    def run_segmented():
+        kda.kda_prefill_segmented(sin.q, sin.k, sin.v, sin.log_alpha, sin.beta, S0=None,
+                                  segments=0, o=o, S_final=Sf, workspace=ws_seg, stream=stream)
+
     steps = max(args.steps, 20)
-    for _ in range(max(args.warmup, 3)):
-        run()
-    torch.cuda.synchronize(dev)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(steps)]
-    barrier(world)
-    torch.cuda.synchronize(dev)
-    with ClockSampler(smi_id) as clk, torch.cuda.stream(stream):
-        for s, e in ev:
-            flush.fill_(1)
-            s.record(stream)
-            run()
-            e.record(stream)
+
+    def timed(fn, wsb):
+        for _ in range(max(args.warmup, 3)):
+            fn()
         torch.cuda.synchronize(dev)
-    barrier(world)
-    check_status_words(ws, ws_.name)
-    times = sorted(s.elapsed_time(e) for s, e in ev)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        with ClockSampler(smi_id) as clk, torch.cuda.stream(stream):
+            for s, e in ev:
+                flush.fill_(1)
+                s.record(stream)
+                fn()
+                e.record(stream)
+            torch.cuda.synchronize(dev)
+        barrier(world)
+        check_status_words(wsb, ws_.name)
+        return sorted(s.elapsed_time(e) for s, e in ev), clk
+
+    times, clk = timed(run, ws)
+    seg_times, _ = timed(run_segmented, ws_seg)
     ms = sum(times)
     ms_max = max_over_ranks(ms, world, dev)
     alg_bytes = T * H * BYTES_PER_TOKEN_HEAD + H * state_bytes(d)       # + the S_final write
@@ -602,9 +613,17 @@ def bench_short(args, kda, torch, synth, peaks, stream, dev, rank, world, smi_id
                      "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                      "traffic": None, "peak_source": peaks["source"], "kernel": kernel,
                      "algorithmic_bytes_per_launch": alg_bytes},
-        # per call: the work-list kernel + the tensor-core kernel
-        "gpu_launches": 2 * steps,
+        # per call: the work-list kernel + the tensor-core kernel; the
+        # segmented call adds the scan and the fix-up
+        "gpu_launches": 2 * steps + 4 * steps,
         "clocks": clk.summary(),
+        # the same prompt through kda_prefill_segmented (chunk-group parallel
+        # prefill, segments chosen by the library; same results)
+        "segmented": {"ms_per_step": sum(seg_times) / steps,
+                      "ms_median": seg_times[len(seg_times) // 2],
+                      "tokens_per_s": T * steps / (sum(seg_times) / 1e3),
+                      "speedup_vs_kda_prefill": sum(times) / sum(seg_times),
+                      "workspace_bytes": int(ws_seg.numel())},
     }
 
 

@@ -32,7 +32,8 @@ KDA_BF16, KDA_FP32, KDA_BF16_F32OUT = 0, 1, 2
 EXPORTS = ("kda_prefill_workspace_bytes", "kda_prefill", "kda_decode_step",
            "kda_status_string", "kda_prefill_noalloc", "kda_prefill_snapshots",
            "kda_decode_multi", "kda_state_gather", "kda_prefill_fused",
-           "kda_decode_step_fused", "kda_prefill_host_staging_bytes", "kda_prefill_host")
+           "kda_decode_step_fused", "kda_prefill_host_staging_bytes", "kda_prefill_host",
+           "kda_prefill_segmented_workspace_bytes", "kda_prefill_segmented")
 
 
 class KdaError(RuntimeError):
@@ -79,6 +80,11 @@ def _declare(lib):
                                      ctypes.c_int, _vp, _vp, _vp]
     lib.kda_state_gather.restype = ctypes.c_int
     lib.kda_state_gather.argtypes = [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp]
+    lib.kda_prefill_segmented_workspace_bytes.restype = _sz
+    lib.kda_prefill_segmented_workspace_bytes.argtypes = [_i64, _i32, _i32, _i32, _i32]
+    lib.kda_prefill_segmented.restype = ctypes.c_int
+    lib.kda_prefill_segmented.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i32, _i32, _i32,
+                                          ctypes.c_int, _vp, _vp, _i32, _vp, _sz, _vp]
     lib.kda_prefill_snapshots.restype = ctypes.c_int
     lib.kda_prefill_snapshots.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                           _i32, _i64, _i32, _i32, _i32, ctypes.c_int,
@@ -197,6 +203,52 @@ def kda_prefill(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, *,
             _stream_handle(stream, dev))
     if rc != KDA_OK:
         raise KdaError(rc, "kda_prefill")
+    return o, S_final
+
+
+def kda_prefill_segmented_workspace_bytes(T: int, H: int, d_k: int, d_v: int,
+                                          segments: int = 0) -> int:
+    return int(lib().kda_prefill_segmented_workspace_bytes(T, H, d_k, d_v, segments))
+
+
+def kda_prefill_segmented(q, k, v, log_alpha, beta, S0=None, *, segments=0, o=None,
+                          S_final=None, want_state=True, workspace=None, stream=None,
+                          o_dtype=None):
+    """Chunk-group parallel prefill of ONE sequence (C ABI:
+    kda_prefill_segmented): the sequence's chunks in ``segments`` groups that
+    run at once (<= 0: chosen by the library), joined by a scan of the
+    segment states and a fix-up of the outputs.  Same arguments and results as
+    kda_prefill with N = 1.  Returns (o, S_final)."""
+    torch = _torch()
+    T, H, dk = q.shape
+    dv = v.shape[2]
+    if o_dtype is None:
+        o_dtype = o.dtype if o is not None else q.dtype
+    dt = _dtype_code(q, o_dtype)
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _check_cuda(name, t, q.dtype)
+    _check_cuda("log_alpha", log_alpha, torch.float32)
+    _check_cuda("beta", beta, torch.float32)
+    _check_cuda("S0", S0, torch.float32)
+    dev = q.device
+    if o is None:
+        o = torch.empty((T, H, dv), dtype=o_dtype, device=dev)
+    _check_cuda("o", o, o_dtype)
+    if S_final is None and want_state:
+        S_final = torch.empty((1, H, dk, dv), dtype=torch.float32, device=dev)
+    _check_cuda("S_final", S_final, torch.float32)
+    with torch.cuda.device(dev):
+        need = kda_prefill_segmented_workspace_bytes(T, H, dk, dv, segments)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    _check_cuda("workspace", workspace)
+    with torch.cuda.device(dev):
+        rc = lib().kda_prefill_segmented(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(S0), T, H, dk, dv, dt,
+            _ptr(o), _ptr(S_final), int(segments), _ptr(workspace),
+            workspace.numel() * workspace.element_size(), _stream_handle(stream, dev))
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_prefill_segmented")
     return o, S_final
 
 

@@ -110,9 +110,10 @@ kda_status_t prefill_impl(const void* q, const void* k, const void* v, const flo
         if (err != cudaSuccess) return KDA_ERR_CUDA;
     }
     if (split) {
+        const kda::SegArgs no_seg{0, 0, nullptr, nullptr};
         err = kda::launch_prefill_split(q, k, v, log_alpha, beta, S0, cu_seqlens, num_seqs,
                                         total_tokens, H, dtype, o, S_final, ws, plan, snap, gate,
-                                        stream);
+                                        no_seg, stream);
         if (err == cudaSuccess) return KDA_OK;
         // The launch was refused (a configuration error, nothing ran): the
         // single-CTA kernel computes the same result.
@@ -144,6 +145,96 @@ kda_status_t kda_prefill(const void* q, const void* k, const void* v,
     const kda::GateArgs given{nullptr, 1.f};
     return prefill_impl(q, k, v, log_alpha, beta, S0, cu_seqlens, num_seqs, total_tokens, H, d_k,
                         d_v, dtype, o, S_final, none, given, workspace, workspace_bytes, stream);
+}
+
+namespace {
+
+// The number of segments kda_prefill_segmented uses for `requested` (<= 0:
+// automatic); 1 means the sequence is not cut.  An explicit request is used
+// when it is possible: every segment non-empty, the consumer units (H (2G - 1))
+// at most half of the SMs.  The automatic choice keeps the units to about a
+// third of the SMs and the segments to at least 24 chunks: more units leave
+// too few producers, shorter segments too little chain to save.  Measured on
+// one GB300 (152 SMs), one sequence, against kda_prefill: H = 16 (2
+// segments) 4 % faster at 4,096 tokens and 18 % at 16,384; H = 8 (3
+// segments) 2.3x at 65,536; H = 4 (6 segments) 3.1x at 32,768; H = 24 and
+// H = 16 at 2,048 tokens slower, so not cut.
+int32_t resolve_segments(int64_t T, int32_t H, int32_t requested, int sms, kda::SegPlan* plan)
+{
+    const long long nch = (T + 63) / 64;
+    if (requested > 0) {
+        if (requested >= 2 && kda::seg_plan(T, H, requested, sms, plan)) return requested;
+        return 1;
+    }
+    const int units_budget = sms * 8 / 25;
+    int32_t G = 1;
+    while (kda::seg_units(H, G + 1) <= units_budget && nch / (G + 1) >= 24) ++G;
+    for (; G >= 2; --G)
+        if (kda::seg_plan(T, H, G, sms, plan)) return G;
+    return 1;
+}
+
+}  // namespace
+
+size_t kda_prefill_segmented_workspace_bytes(int64_t total_tokens, int32_t H, int32_t d_k,
+                                             int32_t d_v, int32_t segments)
+{
+    kda::SegPlan plan;
+    if (d_k == 128 && d_v == 128 && H >= 1 && total_tokens >= 1 &&
+        resolve_segments(total_tokens, H, segments, kda::device_sm_count(), &plan) >= 2)
+        return plan.bytes;
+    return kda_prefill_workspace_bytes(1, H, d_k, d_v);
+}
+
+kda_status_t kda_prefill_segmented(const void* q, const void* k, const void* v,
+                                   const float* log_alpha, const float* beta, const float* S0,
+                                   int64_t total_tokens, int32_t H, int32_t d_k, int32_t d_v,
+                                   kda_dtype_t dtype, void* o, float* S_final, int32_t segments,
+                                   void* workspace, size_t workspace_bytes, cudaStream_t stream)
+{
+    kda::SegPlan plan;
+    const bool tc = (dtype == KDA_BF16 || dtype == KDA_BF16_F32OUT) && d_k == 128 && d_v == 128 &&
+                    kda::prefill_tc_supported(dtype, d_k, total_tokens);
+    const int32_t G = (tc && H >= 1 && total_tokens >= 1)
+                          ? resolve_segments(total_tokens, H, segments, kda::device_sm_count(), &plan)
+                          : 1;
+    if (G < 2 || workspace_bytes < plan.bytes)
+        // Not worth (or not possible) to cut: the plain prefill, same results.
+        return kda_prefill(q, k, v, log_alpha, beta, S0, nullptr, 1, total_tokens, H, d_k, d_v,
+                           dtype, o, S_final, workspace, workspace_bytes, stream);
+    // Argument checks of kda_prefill (one sequence).
+    if (total_tokens > INT32_MAX) return KDA_ERR_INVALID_ARG;
+    if (!q || !k || !v || !log_alpha || !beta || !o) return KDA_ERR_INVALID_ARG;
+    const void* ptrs16[] = {q, k, v, log_alpha, o, S0, S_final};
+    for (const void* p : ptrs16)
+        if (p && !aligned(p, 16)) return KDA_ERR_INVALID_ARG;
+    if (!aligned(beta, 4)) return KDA_ERR_INVALID_ARG;
+    const size_t state_bytes = (size_t)H * d_k * d_v * sizeof(float);
+    if (S0 && S_final && S0 != S_final && overlaps(S0, state_bytes, S_final, state_bytes))
+        return KDA_ERR_INVALID_ARG;
+    if (S_final && overlaps(o, (size_t)total_tokens * H * d_v * out_bytes(dtype), S_final, state_bytes))
+        return KDA_ERR_INVALID_ARG;
+    if (!workspace || !aligned(workspace, 256)) return KDA_ERR_WORKSPACE;
+
+    uint8_t* wsb = static_cast<uint8_t*>(workspace);
+    int32_t* ws = reinterpret_cast<int32_t*>(wsb);
+    const kda::SplitPlan& sp = plan.split;
+    const kda::SnapArgs none{0, nullptr, nullptr};
+    const kda::GateArgs given{nullptr, 1.f};
+    const kda::SegArgs seg{G, plan.seg_chunks, reinterpret_cast<__half*>(wsb + plan.o_aux_off),
+                           reinterpret_cast<float*>(wsb + plan.st_aux_off)};
+    int32_t* flags = reinterpret_cast<int32_t*>(wsb + sp.flags_off);
+    const int32_t nflags = sp.groups * sp.ring + sp.units;
+    cudaError_t err = kda::launch_worklist(nullptr, 1, total_tokens, ws, flags, nflags, none, stream);
+    if (err != cudaSuccess) return KDA_ERR_CUDA;
+    // S_final may alias S0: segment 0 has read S0 before the scan writes it.
+    err = kda::launch_prefill_split(q, k, v, log_alpha, beta, S0, nullptr, 1, total_tokens, H, dtype,
+                                    o, nullptr, ws, sp, none, given, seg, stream);
+    if (err != cudaSuccess) return KDA_ERR_CUDA;
+    err = kda::launch_segment_fixup(seg, total_tokens, H, dtype, o, S_final,
+                                    reinterpret_cast<__half*>(wsb + plan.sstart_off),
+                                    ws + kda::kWsTimeoutWord, stream);
+    return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
 kda_status_t kda_prefill_snapshots(const void* q, const void* k, const void* v,

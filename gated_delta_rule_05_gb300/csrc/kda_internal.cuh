@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <stdlib.h>
@@ -49,6 +50,7 @@ constexpr int kSplitMaxRing = 32;
 
 struct SplitPlan {
     int32_t units, producers, ring;
+    int32_t groups;       // ring groups (one per unit, or per segment and head)
     size_t flags_off, ring_off, bytes;
 };
 
@@ -73,10 +75,105 @@ inline bool split_plan(int32_t num_seqs, int32_t H, int sms, SplitPlan* plan) {
     p.ring = 3 * ahead + 4;
     if (p.ring < 4) p.ring = 4;
     if (p.ring > kSplitMaxRing) p.ring = kSplitMaxRing;
+    p.groups = p.units;
     p.flags_off = workspace_bytes(num_seqs);
     const size_t nflags = (size_t)p.units * (p.ring + 1);
     p.ring_off = (p.flags_off + nflags * sizeof(int32_t) + 1023) / 1024 * 1024;
     p.bytes = p.ring_off + (size_t)p.units * p.ring * 2 * kSplitStepBytes;
+    *plan = p;
+    return true;
+}
+
+// Chunk-group parallel prefill of one sequence (kda_prefill_segmented): the
+// sequence is cut into G segments of seg_chunks chunks.  Segment 0 runs from
+// the caller's S0 and writes the final outputs.  Every later segment g runs
+// twice on the producers' shared operands: a local run from S = 0 (outputs
+// o_loc, final state L_g) and an identity run with v = 0 from S = I (outputs
+// qt = Phi_t^T q_t, final state M_g = Phi_g, the segment's transition).  By
+// linearity the true state entering segment g is S_g = M_{g-1} S_{g-1} +
+// L_{g-1} (S_1 = L_0) and the true output is o_t = o_loc,t + S_g^T qt_t.
+struct SegArgs {
+    int32_t G;            // segments (1 or less: not segmented)
+    int32_t seg_chunks;   // chunks per segment (even: segments are whole 128-token tiles)
+    __half* o_aux;        // [2][T][H][d_v] fp16: o_loc, qt (segments >= 1)
+    float* st_aux;        // [2][G][H][d_k][d_v] fp32: L_g, M_g (L_0: segment 0's state)
+};
+
+// Consumer units of a segmented launch: H units of segment 0 (mode 0), then
+// per later segment H local units (mode 1) and H identity units (mode 2).
+struct SegUnit {
+    int g, mode, h;
+};
+
+__host__ __device__ __forceinline__ int seg_units(int H, int G) { return H * (2 * G - 1); }
+
+__host__ __device__ __forceinline__ SegUnit seg_unit(int u, int H)
+{
+    SegUnit r;
+    if (u < H) {
+        r.g = 0;
+        r.mode = 0;
+        r.h = u;
+        return r;
+    }
+    const int v = u - H;
+    r.g = 1 + v / (2 * H);
+    r.mode = 1 + (v % (2 * H)) / H;
+    r.h = v % H;
+    return r;
+}
+
+// The consumer units that read ring group (g, h): one for segment 0, two after.
+__host__ __device__ __forceinline__ int seg_group_consumers(int g, int h, int H, int (&u)[2])
+{
+    if (g == 0) {
+        u[0] = h;
+        return 1;
+    }
+    u[0] = H + (g - 1) * 2 * H + h;
+    u[1] = u[0] + H;
+    return 2;
+}
+
+// Workspace of kda_prefill_segmented: the work list, the split kernel's flags
+// (full[groups][ring], consumed[units]) and ring, then o_aux, st_aux and the
+// segment entry states S_g, transposed to fp16 in the 128-byte swizzled
+// K-major layout of an MMA operand ([G][H] blocks of 32 KB), written by the
+// scan for the fix-up's tensor-core product.
+struct SegPlan {
+    SplitPlan split;
+    int32_t G, seg_chunks;
+    size_t o_aux_off, st_aux_off, sstart_off, bytes;
+};
+
+inline bool seg_plan(int64_t T, int32_t H, int32_t G, int sms, SegPlan* plan)
+{
+    if (T < 1 || H < 1 || G < 2 || sms < 3) return false;
+    const long long nch = (T + 63) / 64;
+    SegPlan p;
+    p.G = G;
+    p.seg_chunks = (int32_t)((nch + G - 1) / G);
+    p.seg_chunks += p.seg_chunks & 1;              // whole 128-token tiles
+    if ((long long)(G - 1) * p.seg_chunks >= nch) return false;   // every segment has a chunk
+    const long long units = (long long)seg_units(H, G);
+    if (units > sms / 2) return false;
+    SplitPlan& s = p.split;
+    s.units = (int32_t)units;
+    s.groups = G * H;
+    s.producers = sms - s.units;
+    const int ahead = (s.producers + s.groups - 1) / s.groups;
+    s.ring = 3 * ahead + 4;
+    if (s.ring > kSplitMaxRing) s.ring = kSplitMaxRing;
+    s.flags_off = workspace_bytes(1);
+    const size_t nflags = (size_t)s.groups * s.ring + s.units;
+    s.ring_off = (s.flags_off + nflags * sizeof(int32_t) + 1023) / 1024 * 1024;
+    s.bytes = s.ring_off + (size_t)s.groups * s.ring * 2 * kSplitStepBytes;
+    const size_t state = (size_t)H * 128 * 128 * sizeof(float);
+    p.o_aux_off = (s.bytes + 255) / 256 * 256;
+    p.st_aux_off = p.o_aux_off + 2 * (size_t)T * H * 128 * sizeof(__half);
+    p.st_aux_off = (p.st_aux_off + 255) / 256 * 256;
+    p.sstart_off = p.st_aux_off + 2 * (size_t)G * state;
+    p.bytes = p.sstart_off + (size_t)G * state / 2;
     *plan = p;
     return true;
 }
@@ -174,6 +271,13 @@ cudaError_t launch_prefill_split(const void* q, const void* k, const void* v,
                                  const int32_t* cu_seqlens, int32_t num_seqs,
                                  int64_t total_tokens, int32_t H, kda_dtype_t dtype, void* o,
                                  float* S_final, int32_t* ws, const SplitPlan& plan,
-                                 const SnapArgs& snap, const GateArgs& gate, cudaStream_t stream);
+                                 const SnapArgs& snap, const GateArgs& gate, const SegArgs& seg,
+                                 cudaStream_t stream);
+
+// The segmented prefill's second pass: the scan over segments (S_g, and the
+// caller's S_final) and the output fix-up o_t += S_g^T qt_t for segments >= 1.
+cudaError_t launch_segment_fixup(const SegArgs& seg, int64_t total_tokens, int32_t H,
+                                 kda_dtype_t dtype, void* o, float* S_final, __half* sstart,
+                                 int32_t* timeout_word, cudaStream_t stream);
 
 }  // namespace kda

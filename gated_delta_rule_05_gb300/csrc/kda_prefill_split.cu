@@ -136,17 +136,20 @@ __device__ __forceinline__ bool global_abort(const Ctx& X)
 }
 
 // ------------------------------------------------------------- consumer
-template <typename TO>
+// SEG: a segmented launch (kda_prefill_segmented); the plain instantiations
+// carry none of its bookkeeping.
+template <typename TO, bool SEG>
 __device__ __forceinline__ void consumer(const Ctx& X, uint32_t tmem, int warp, int lane,
                                          const CUtensorMap* tm_v, const CUtensorMap* tm_o,
                                          const float* S0, const int32_t* cu, const int32_t* ws,
                                          long long total_tokens, int H, TO* o, float* S_final,
                                          int U, int R, int32_t* flags, const uint8_t* ring,
-                                         const SnapArgs& snap)
+                                         const SnapArgs& snap, const SegArgs& seg,
+                                         const CUtensorMap* tm_aux0, const CUtensorMap* tm_aux1)
 {
     uint8_t* sm = X.sm;
     const int u = blockIdx.x;
-    const int rank = u / H, h = u % H;
+    int rank = u / H, h = u % H;
     long long bos = 0, eos = total_tokens;
     int n = 0;
     if (cu != nullptr) {
@@ -154,11 +157,34 @@ __device__ __forceinline__ void consumer(const Ctx& X, uint32_t tmem, int warp, 
         bos = cu[n];
         eos = cu[n + 1];
     }
+    // Segmented launch (one sequence): this unit's segment, its mode (0: the
+    // first segment, from S0 into o; 1: a later segment from S = 0 into the
+    // local outputs; 2: its identity run, v = 0 from S = I) and its ring group
+    // (segment, head), which the local and identity units share.
+    int mode = 0, group = u, groups = U;
+    __half* o_aux = nullptr;
+    float* s_dst = S_final;
+    long long sdst_base = 0;
+    if (SEG) {
+        const SegUnit su = seg_unit(u, H);
+        h = su.h;
+        mode = su.mode;
+        group = su.g * H + su.h;
+        groups = seg.G * H;
+        bos = (long long)su.g * seg.seg_chunks * kC;
+        eos = bos + (long long)seg.seg_chunks * kC;
+        if (eos > total_tokens) eos = total_tokens;
+        if (mode > 0) o_aux = seg.o_aux + (size_t)(mode - 1) * total_tokens * H * kD;
+        s_dst = seg.st_aux + (size_t)(mode == 2 ? seg.G : 0) * H * kD * kD;
+        sdst_base = ((long long)su.g * H + h) * kD * kD;
+    }
     const int nch = (int)((eos - bos + kC - 1) / kC);
     const long long sbase = ((long long)n * H + h) * kD * kD;
-    const int32_t* full = flags + (size_t)u * R;
-    int32_t* consumed = flags + (size_t)U * R + u;
-    const uint8_t* uring = ring + (size_t)u * R * 2 * kStage;
+    if (!SEG) sdst_base = sbase;
+    const bool with_v = !SEG || mode != 2;
+    const int32_t* full = flags + (size_t)group * R;
+    int32_t* consumed = flags + (size_t)groups * R + u;
+    const uint8_t* uring = ring + (size_t)group * R * 2 * kStage;
 
     if (warp == 0) {
         // ------------------------------------------------------ loader
@@ -178,9 +204,9 @@ __device__ __forceinline__ void consumer(const Ctx& X, uint32_t tmem, int warp, 
             ++issued_v[vb];
             return true;
         };
-        for (int cv = 0; cv < kVAhead && cv < nch; ++cv) issue_v(cv);
+        for (int cv = 0; cv < kVAhead && cv < nch && with_v; ++cv) issue_v(cv);
         for (int c = 0; c < nch && ok; ++c) {
-            if (c + kVAhead < nch && !issue_v(c + kVAhead)) { ok = false; break; }
+            if (with_v && c + kVAhead < nch && !issue_v(c + kVAhead)) { ok = false; break; }
             const int slot = c % R;
             int32_t val = 0;
             // Relaxed polls: an acquire load would also wait for this warp's
@@ -248,9 +274,9 @@ __device__ __forceinline__ void consumer(const Ctx& X, uint32_t tmem, int warp, 
             // the warp's products in flight; 46 % from a compute thread; 6 %
             // from an eleventh warp that did nothing else.)
             if (d.last_pass && lane == 0) red_max_relaxed_gpu(consumed, d.chunk + 1);
-            mma_back_c(tmem, blk + BLK_WT, blk + BLK_T16, smem_u32(sm + C_V0 + vb * 16384));
+            mma_back_c(tmem, blk + BLK_WT, blk + BLK_T16, smem_u32(sm + C_V0 + vb * 16384), with_v);
             mma_commit(&X.bar[B_MMA_C]);
-            if (d.last_pass) mma_commit(&X.bar[B_SV_EMPTY0 + vb]);
+            if (d.last_pass && with_v) mma_commit(&X.bar[B_SV_EMPTY0 + vb]);
             if (!warp_wait(X, B_U, step)) break;
             tc_fence_after();
             mma_back_os(tmem, blk + BLK_P);
@@ -268,13 +294,19 @@ __device__ __forceinline__ void consumer(const Ctx& X, uint32_t tmem, int warp, 
         // chunk's v tile to fp16.
         const Lane t = make_lane(threadIdx.x - 64, warp, lane);
         const int seq_off = (cu != nullptr && snap.interval > 0) ? snap.offsets[n] : 0;
-        state_load(t, tmem, S0, sbase);
+        state_load(t, tmem, mode == 0 ? S0 : nullptr, sbase, mode == 2);
         bool alive = nch > 0;
         StepDesc prev;
         prev.t0 = 0;
         prev.lo = prev.hi = 0;
         int step = 0;
         auto store_prev_o = [&](const uint32_t (&dd)[32]) {
+            if (SEG && o_aux != nullptr) {   // a later segment's run: fp16, through its own map
+                const bool tma_aux = prev.lo == 0 && prev.hi == kC;
+                o_store<__half>(t, dd, tma_aux, mode == 1 ? tm_aux0 : tm_aux1, sm + C_OST, o_aux,
+                                (long long)prev.t0, prev.lo, prev.hi, h, H);
+                return;
+            }
             const bool tma_out = (sizeof(TO) == 2) && prev.lo == 0 && prev.hi == kC;
             o_store<TO>(t, dd, tma_out, tm_o, sm + C_OST, o, (long long)prev.t0, prev.lo, prev.hi,
                         h, H);
@@ -287,7 +319,7 @@ __device__ __forceinline__ void consumer(const Ctx& X, uint32_t tmem, int warp, 
             fence_proxy_async_smem();
             return true;
         };
-        if (alive) alive = convert_v(0);
+        if (alive && with_v) alive = convert_v(0);
         while (alive) {
             const int s = step & 1;
             if (!group_wait(X, B_ST_FULL0 + s, step >> 1)) { alive = false; break; }
@@ -312,7 +344,7 @@ __device__ __forceinline__ void consumer(const Ctx& X, uint32_t tmem, int warp, 
             tc_fence_before();
             group_sync();
             if (t.ct == 0) mbar_arrive(&X.bar[B_U]);
-            if (d.last_pass && d.chunk + 1 < nch && !convert_v(d.chunk + 1)) { alive = false; break; }
+            if (with_v && d.last_pass && d.chunk + 1 < nch && !convert_v(d.chunk + 1)) { alive = false; break; }
             ++step;
             if (d.last_step) break;
         }
@@ -329,7 +361,7 @@ __device__ __forceinline__ void consumer(const Ctx& X, uint32_t tmem, int warp, 
         // (A wait that gave up has set the abort flag; a unit without chunks
         // stores its S0.)
         if (!*reinterpret_cast<volatile int32_t*>(&X.misc->abort)) {
-            if (S_final) state_store(t, tmem, S_final, sbase);
+            if (s_dst) state_store(t, tmem, s_dst, sdst_base);
             float* last = snapshot_at(snap, nch, eos - bos, seq_off, H, h);
             if (last) state_store(t, tmem, last, 0);
         }
@@ -337,14 +369,17 @@ __device__ __forceinline__ void consumer(const Ctx& X, uint32_t tmem, int warp, 
 }
 
 // ------------------------------------------------------------- producer
-template <typename TO, bool FUSED>
+template <typename TO, bool FUSED, bool SEG>
 __device__ __forceinline__ void producer(const Ctx& X, uint32_t tmem, int warp, int lane,
                                          const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                                          const CUtensorMap* tm_g, const float* beta,
                                          const int32_t* cu, int32_t* ws, long long total_tokens,
                                          int H, int U, int R, int32_t* flags, uint8_t* ring,
-                                         const GateArgs& gate)
+                                         const GateArgs& gate, const SegArgs& seg)
 {
+    // Ring groups: one per consumer unit, or (segmented) one per segment and
+    // head, read by that segment's one or two consumer units.
+    const int groups = SEG ? seg.G * H : U;
     uint8_t* sm = X.sm;
     JobDesc* jd = reinterpret_cast<JobDesc*>(sm + OFF_JOB);
     if (warp == 0) {
@@ -356,7 +391,10 @@ __device__ __forceinline__ void producer(const Ctx& X, uint32_t tmem, int warp, 
         }
         float* sBin = reinterpret_cast<float*>(sm + OFF_BIN);
         const long long maxlen = (cu != nullptr) ? ws[kWsMaxLenWord] : total_tokens;
-        const long long total_jobs = (long long)U * ((maxlen + kC - 1) / kC);
+        // Segmented: jobs in order of the chunk index within the segment, so
+        // that every segment's chain starts at once.
+        const long long total_jobs = SEG ? (long long)seg.G * H * seg.seg_chunks
+                                         : (long long)U * ((maxlen + kC - 1) / kC);
         unsigned long long* counter = reinterpret_cast<unsigned long long*>(ws + kWsJobWord);
         const int32_t* order = ws + kWsHeaderBytes / sizeof(int32_t);
         int2* seq_tab = reinterpret_cast<int2*>(sm + P_SEQ);
@@ -394,16 +432,25 @@ __device__ __forceinline__ void producer(const Ctx& X, uint32_t tmem, int warp, 
                         uu = -1;
                         break;
                     }
-                    c = (int)(j / U);
-                    uu = (int)(j % U);
-                    hh = uu % H;
-                    if (cu != nullptr) {
-                        const int2 se = seq_tab[uu / H];
-                        bos = se.x;
-                        eos = se.y;
+                    if (SEG) {
+                        c = (int)(j / ((long long)seg.G * H));
+                        uu = (int)(j % ((long long)seg.G * H));     // the group: segment, head
+                        hh = uu % H;
+                        bos = (long long)(uu / H) * seg.seg_chunks * kC;
+                        eos = bos + (long long)seg.seg_chunks * kC;
+                        if (eos > total_tokens) eos = total_tokens;
                     } else {
-                        bos = 0;
-                        eos = total_tokens;
+                        c = (int)(j / U);
+                        uu = (int)(j % U);
+                        hh = uu % H;
+                        if (cu != nullptr) {
+                            const int2 se = seq_tab[uu / H];
+                            bos = se.x;
+                            eos = se.y;
+                        } else {
+                            bos = 0;
+                            eos = total_tokens;
+                        }
                     }
                     if ((long long)c * kC < eos - bos) break;   // else: this unit has no chunk c
                 }
@@ -478,7 +525,7 @@ __device__ __forceinline__ void producer(const Ctx& X, uint32_t tmem, int warp, 
         // ------------------------------------------------ compute group
         const Lane t = make_lane(threadIdx.x - 64, warp, lane);
         const int ct = t.ct;
-        const int32_t* consumed = flags + (size_t)U * R;
+        const int32_t* consumed = flags + (size_t)groups * R;
         int step = 0;
         // Job jc - 1 is handed to the data-movement warp (JOB_DONE) during
         // job jc, once pass B is done: by then ct 0's last bulk copies have
@@ -509,7 +556,16 @@ __device__ __forceinline__ void producer(const Ctx& X, uint32_t tmem, int warp, 
             // The slot is free once the consumer has copied out chunk c - R.
             // A first look is issued now and checked after pass B.
             const int32_t want = job.c - R + 1;
-            int32_t seen = (ct == 0 && job.c >= R) ? ld_relaxed_gpu(consumed + job.u) : want;
+            // The group's consumer units (two in a later segment of a
+            // segmented launch: the slot is free once both have copied it).
+            int cons[2] = {job.u, job.u};
+            int ncons = 1;
+            if (SEG) ncons = seg_group_consumers(job.u / H, job.u % H, H, cons);
+            int32_t seen = want;
+            if (ct == 0 && job.c >= R) {
+                seen = ld_relaxed_gpu(consumed + cons[0]);
+                if (ncons > 1) seen = min(seen, ld_relaxed_gpu(consumed + cons[1]));
+            }
             float2 Gq[16];
             PassParams pp;
             if (FUSED) qk_norms(X, t, gate.q_scale);
@@ -540,9 +596,11 @@ __device__ __forceinline__ void producer(const Ctx& X, uint32_t tmem, int warp, 
                         // look into an acquire (the poll's loads already
                         // are), and the proxy fence orders the bulk stores
                         // below after it.
-                        if (seen < want)
-                            free_slot = poll_flag(X, consumed + job.u,
-                                                  [&](int32_t v) { return v >= want; }, &seen);
+                        for (int ci = 0; ci < ncons && free_slot && seen < want; ++ci) {
+                            int32_t sc = 0;
+                            free_slot = poll_flag(X, consumed + cons[ci],
+                                                  [&](int32_t v) { return v >= want; }, &sc);
+                        }
                         fence_acquire_gpu();
                         fence_proxy_async_global();
                     }
@@ -583,16 +641,19 @@ __device__ __forceinline__ void producer(const Ctx& X, uint32_t tmem, int warp, 
 }
 
 // ------------------------------------------------------------- the kernel
-// FUSED: the gate prologue runs in the producers (gate.A not null).
-template <typename TO, bool FUSED>
+// FUSED: the gate prologue runs in the producers (gate.A not null).  SEG: a
+// segmented launch (seg.G > 1).
+template <typename TO, bool FUSED, bool SEG>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_split_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUtensorMap tm_v,
-                     const __grid_constant__ CUtensorMap tm_o, const float* __restrict__ beta,
+                     const __grid_constant__ CUtensorMap tm_o,
+                     const __grid_constant__ CUtensorMap tm_aux0,
+                     const __grid_constant__ CUtensorMap tm_aux1, const float* __restrict__ beta,
                      const float* S0, const int32_t* __restrict__ cu, int32_t* ws,
                      long long total_tokens, int H, TO* __restrict__ o, float* S_final, int U, int R,
                      int32_t* flags, uint8_t* ring, const SnapArgs snap, const GateArgs gate,
-                     int test_starve)
+                     const SegArgs seg, int test_starve)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -623,11 +684,11 @@ prefill_split_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     const uint32_t tmem = X.misc->tmem_base;
 
     if ((int)blockIdx.x < U)
-        consumer<TO>(X, tmem, warp, lane, &tm_v, &tm_o, S0, cu, ws, total_tokens, H, o, S_final, U,
-                     R, flags, ring, snap);
+        consumer<TO, SEG>(X, tmem, warp, lane, &tm_v, &tm_o, S0, cu, ws, total_tokens, H, o, S_final, U,
+                     R, flags, ring, snap, seg, &tm_aux0, &tm_aux1);
     else if (!test_starve)
-        producer<TO, FUSED>(X, tmem, warp, lane, &tm_q, &tm_k, &tm_g, beta, cu, ws, total_tokens, H, U,
-                        R, flags, ring, gate);
+        producer<TO, FUSED, SEG>(X, tmem, warp, lane, &tm_q, &tm_k, &tm_g, beta, cu, ws, total_tokens, H, U,
+                        R, flags, ring, gate, seg);
 
     tc_fence_before();
     __syncthreads();
@@ -637,11 +698,12 @@ prefill_split_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     }
 }
 
-template <typename TO, bool FUSED>
+template <typename TO, bool FUSED, bool SEG>
 cudaError_t launch_typed(const void* q, const void* k, const void* v, const float* g,
                          const float* beta, const float* S0, const int32_t* cu, int64_t T,
                          int32_t H, void* o, float* S_final, int32_t* ws, const SplitPlan& plan,
-                         const SnapArgs& snap, const GateArgs& gate, cudaStream_t stream)
+                         const SnapArgs& snap, const GateArgs& gate, const SegArgs& seg,
+                         cudaStream_t stream)
 {
     CUtensorMap mq, mk, mg, mv, mo;
     const bool bf16_out = sizeof(TO) == 2;
@@ -653,7 +715,15 @@ cudaError_t launch_typed(const void* q, const void* k, const void* v, const floa
         !tc_make_map(&mv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, T, 64, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     if (!bf16_out) mo = mq;
-    auto kern = prefill_split_kernel<TO, FUSED>;
+    // A segmented launch's fp16 outputs of the later segments' two runs.
+    CUtensorMap ma0 = mq, ma1 = mq;
+    if (seg.G > 1 &&
+        (!tc_make_map(&ma0, seg.o_aux, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, H, T, kD,
+                      CU_TENSOR_MAP_SWIZZLE_NONE) ||
+         !tc_make_map(&ma1, seg.o_aux + (size_t)T * H * kD, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, H,
+                      T, kD, CU_TENSOR_MAP_SWIZZLE_NONE)))
+        return cudaErrorInvalidValue;
+    auto kern = prefill_split_kernel<TO, FUSED, SEG>;
     static bool attr_set = false;   // benign race: every writer stores the same value
     if (!attr_set) {
         const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -680,9 +750,9 @@ cudaError_t launch_typed(const void* q, const void* k, const void* v, const floa
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     const int test_starve = getenv("KDA_TEST_STARVE_CONSUMERS") != nullptr ? 1 : 0;
-    e = cudaLaunchKernelEx(&cfg, kern, mq, mk, mg, mv, mo, beta, S0, cu, ws, (long long)T, (int)H,
+    e = cudaLaunchKernelEx(&cfg, kern, mq, mk, mg, mv, mo, ma0, ma1, beta, S0, cu, ws, (long long)T, (int)H,
                            static_cast<TO*>(o), S_final, (int)plan.units, (int)plan.ring, flags,
-                           ring, snap, gate, test_starve);
+                           ring, snap, gate, seg, test_starve);
     if (e != cudaSuccess && debug_enabled())
         fprintf(stderr, "kda: prefill_split launch failed: %s\n", cudaGetErrorString(e));
     return e;
@@ -695,23 +765,35 @@ cudaError_t launch_prefill_split(const void* q, const void* k, const void* v,
                                  const int32_t* cu_seqlens, int32_t num_seqs,
                                  int64_t total_tokens, int32_t H, kda_dtype_t dtype, void* o,
                                  float* S_final, int32_t* ws, const SplitPlan& plan,
-                                 const SnapArgs& snap, const GateArgs& gate, cudaStream_t stream)
+                                 const SnapArgs& snap, const GateArgs& gate, const SegArgs& seg,
+                                 cudaStream_t stream)
 {
     (void)num_seqs;
     const bool fused = gate.A != nullptr;
+    if (seg.G > 1) {   // segmented launches take no gate prologue
+        if (fused) return cudaErrorInvalidValue;
+        if (dtype == KDA_BF16_F32OUT)
+            return launch_typed<float, false, true>(q, k, v, log_alpha, beta, S0, cu_seqlens,
+                                                    total_tokens, H, o, S_final, ws, plan, snap,
+                                                    gate, seg, stream);
+        return launch_typed<__nv_bfloat16, false, true>(q, k, v, log_alpha, beta, S0, cu_seqlens,
+                                                        total_tokens, H, o, S_final, ws, plan,
+                                                        snap, gate, seg, stream);
+    }
     if (dtype == KDA_BF16_F32OUT)
-        return fused ? launch_typed<float, true>(q, k, v, log_alpha, beta, S0, cu_seqlens,
-                                                 total_tokens, H, o, S_final, ws, plan, snap, gate,
-                                                 stream)
-                     : launch_typed<float, false>(q, k, v, log_alpha, beta, S0, cu_seqlens,
-                                                  total_tokens, H, o, S_final, ws, plan, snap, gate,
-                                                  stream);
-    return fused ? launch_typed<__nv_bfloat16, true>(q, k, v, log_alpha, beta, S0, cu_seqlens,
-                                                     total_tokens, H, o, S_final, ws, plan, snap,
-                                                     gate, stream)
-                 : launch_typed<__nv_bfloat16, false>(q, k, v, log_alpha, beta, S0, cu_seqlens,
-                                                      total_tokens, H, o, S_final, ws, plan, snap,
-                                                      gate, stream);
+        return fused ? launch_typed<float, true, false>(q, k, v, log_alpha, beta, S0, cu_seqlens,
+                                                        total_tokens, H, o, S_final, ws, plan, snap,
+                                                        gate, seg, stream)
+                     : launch_typed<float, false, false>(q, k, v, log_alpha, beta, S0, cu_seqlens,
+                                                         total_tokens, H, o, S_final, ws, plan,
+                                                         snap, gate, seg, stream);
+    return fused ? launch_typed<__nv_bfloat16, true, false>(q, k, v, log_alpha, beta, S0,
+                                                            cu_seqlens, total_tokens, H, o, S_final,
+                                                            ws, plan, snap, gate, seg, stream)
+                 : launch_typed<__nv_bfloat16, false, false>(q, k, v, log_alpha, beta, S0,
+                                                             cu_seqlens, total_tokens, H, o,
+                                                             S_final, ws, plan, snap, gate, seg,
+                                                             stream);
 }
 
 }  // namespace kda

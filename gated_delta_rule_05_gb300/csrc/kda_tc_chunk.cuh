@@ -180,6 +180,7 @@ __device__ __forceinline__ float hi_bf16(uint32_t x) { return __uint_as_float(x 
 
 __device__ __forceinline__ void out_store(float* p, float x) { *p = x; }
 __device__ __forceinline__ void out_store(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
+__device__ __forceinline__ void out_store(__half* p, float x) { *p = __float2half_rn(x); }
 
 // Limit of a bounded wait: 2^32 SM cycles, about two seconds.  (A compile-
 // time constant: a limit held in a register measured 5 % slower at 1M tokens.)
@@ -766,24 +767,26 @@ __device__ __forceinline__ void v_tile_to_f16(uint8_t* vtile, int ct)
 __device__ __forceinline__ void state_decay(const Lane& t, uint32_t tmem, const float* gl,
                                             float* snap = nullptr)
 {
-#pragma unroll
-    for (int jb = 0; jb < 2; ++jb) {
-        const int c0 = 64 * t.half + 32 * jb;
-        uint32_t r[32], b[16];
-        tmem_ld32(tmem + t.lane_base + TM_S + c0, r);
+    // 16 columns at a time: this phase runs while many other values are live,
+    // and wider pieces spilled registers.
+#pragma unroll 1
+    for (int jb = 0; jb < 4; ++jb) {
+        const int c0 = 64 * t.half + 16 * jb;
+        uint32_t r[16], b[8];
+        tmem_ld16(tmem + t.lane_base + TM_S + c0, r);
         tmem_ld_wait();
         if (snap != nullptr) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) snap[(long long)(c0 + i) * kD + t.L] = __uint_as_float(r[i]);
+            for (int i = 0; i < 16; ++i) snap[(long long)(c0 + i) * kD + t.L] = __uint_as_float(r[i]);
         }
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
+        for (int i = 0; i < 8; ++i)
             b[i] = pack_f16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
-        tmem_st16(tmem + t.lane_base + TM_SB + (c0 >> 1), b);
+        tmem_st8(tmem + t.lane_base + TM_SB + (c0 >> 1), b);
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
+        for (int i = 0; i < 16; ++i)
             r[i] = __float_as_uint(__uint_as_float(r[i]) * gl[c0 + i]);
-        tmem_st32(tmem + t.lane_base + TM_S + c0, r);
+        tmem_st16(tmem + t.lane_base + TM_S + c0, r);
     }
     tmem_st_wait();
 }
@@ -809,11 +812,22 @@ __device__ __forceinline__ void o_load(const Lane& t, uint32_t tmem, uint32_t (&
 }
 
 // Stores rows [lo, hi) of a chunk's O (token t0 + r).  A full chunk with bf16
-// output is staged in shared memory (stg, [64 tok][128 v] bf16 plain rows) and
-// written by one TMA tensor store issued by ct 0 (committed to its bulk
-// group; the caller waits for the staging to be read before reusing it);
-// other chunks (a ragged tail, the passes of a wide chunk, fp32 output) are
-// stored by the threads.  `use_tma` must be uniform over the group.
+// output is staged in shared memory (stg, [64 tok][128 v] plain rows of the
+// 16-bit output type) and written by one TMA tensor store issued by ct 0
+// (committed to its bulk group; the caller waits for the staging to be read
+// before reusing it); other chunks (a ragged tail, the passes of a wide chunk,
+// fp32 output) are stored by the threads.  `use_tma` must be uniform over the
+// group, and false for fp32 output.
+__device__ __forceinline__ void stage16(uint8_t* p, float x, const __nv_bfloat16*)
+{
+    *reinterpret_cast<__nv_bfloat16*>(p) = __float2bfloat16_rn(x);
+}
+__device__ __forceinline__ void stage16(uint8_t* p, float x, const __half*)
+{
+    *reinterpret_cast<__half*>(p) = __float2half_rn(x);
+}
+__device__ __forceinline__ void stage16(uint8_t*, float, const float*) {}
+
 template <typename TO>
 __device__ __forceinline__ void o_store(const Lane& t, const uint32_t (&dd)[32], bool use_tma,
                                         const CUtensorMap* tm_o, uint8_t* stg, TO* o, long long t0,
@@ -823,8 +837,7 @@ __device__ __forceinline__ void o_store(const Lane& t, const uint32_t (&dd)[32],
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
             const int r = 32 * t.half + i;
-            *reinterpret_cast<__nv_bfloat16*>(stg + r * 256 + 2 * t.L) =
-                __float2bfloat16_rn(__uint_as_float(dd[i]));
+            stage16(stg + r * 256 + 2 * t.L, __uint_as_float(dd[i]), static_cast<const TO*>(nullptr));
         }
         fence_proxy_async_smem();
         group_sync();
@@ -842,10 +855,10 @@ __device__ __forceinline__ void o_store(const Lane& t, const uint32_t (&dd)[32],
     }
 }
 
-// S^T <- S0^T (row v of S^T is column v of S0), or zeros.  This thread: 64
-// channels of its TMEM lane.
+// S^T <- S0^T (row v of S^T is column v of S0), zeros, or (identity) the
+// unit matrix.  This thread: 64 channels of its TMEM lane.
 __device__ __forceinline__ void state_load(const Lane& t, uint32_t tmem, const float* S0,
-                                           long long sbase)
+                                           long long sbase, bool identity = false)
 {
 #pragma unroll
     for (int jb = 0; jb < 2; ++jb) {
@@ -853,7 +866,9 @@ __device__ __forceinline__ void state_load(const Lane& t, uint32_t tmem, const f
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
             const int c = 64 * t.half + 32 * jb + i;
-            r[i] = __float_as_uint(S0 ? S0[sbase + (long long)c * kD + t.L] : 0.f);
+            const float x = identity ? (c == t.L ? 1.f : 0.f)
+                                     : (S0 ? S0[sbase + (long long)c * kD + t.L] : 0.f);
+            r[i] = __float_as_uint(x);
         }
         tmem_st32(tmem + t.lane_base + TM_S + 64 * t.half + 32 * jb, r);
     }
@@ -936,7 +951,8 @@ __device__ __forceinline__ bool mma_front(const Ctx& X, uint32_t tmem, const Fro
 // [U^T | O^T] = S^T [-W^T | (e^G Q)^T] ;  U^T += V^T T^T.  Shared-memory
 // addresses: wt = -W^T with (e^G Q)^T 16 KB after it, t16 = T (fp16),
 // vtile = the fp16 v tile.
-__device__ __forceinline__ void mma_back_c(uint32_t tmem, uint32_t wt, uint32_t t16, uint32_t vtile)
+__device__ __forceinline__ void mma_back_c(uint32_t tmem, uint32_t wt, uint32_t t16, uint32_t vtile,
+                                           bool with_v = true)
 {
     const uint32_t id_cv = make_idesc_f16(128, 64, true, false);     // V^T T^T
     const uint32_t id_mn128 = make_idesc_f16(128, 128, false, true); // S^T x [-W^T | (e^G Q)^T]
@@ -945,6 +961,7 @@ __device__ __forceinline__ void mma_back_c(uint32_t tmem, uint32_t wt, uint32_t 
     const uint64_t dT16 = make_sdesc(t16, 16, 1024, kSwizzle128B);
 #pragma unroll
     for (int s = 0; s < 8; ++s) mma_ts(tmem + TM_C, tmem + TM_SB + s * 8, dWQ + 128 * s, id_mn128, s > 0);
+    if (!with_v) return;      // v = 0: U^T = -S^T W^T
 #pragma unroll
     for (int s = 0; s < 4; ++s) mma_ss(tmem + TM_C, dV + 128 * s, dT16 + 2 * s, id_cv, 1);
 }

@@ -195,6 +195,55 @@ kda_status_t kda_prefill_fused(const void *q, const void *k, const void *v,
                                void *workspace, size_t workspace_bytes,
                                cudaStream_t stream);
 
+/* Bytes of device workspace kda_prefill_segmented needs for one sequence of
+ * total_tokens tokens and H heads cut into `segments` segments (<= 0: the
+ * number the call would choose).  When the call would not cut the sequence
+ * (see below) this is kda_prefill_workspace_bytes(1, H, d_k, d_v).  The
+ * workspace holds, besides kda_prefill's, two fp32 copies of the outputs
+ * (8 * total_tokens * H * d_v bytes) and 3 * segments states per head. */
+size_t kda_prefill_segmented_workspace_bytes(int64_t total_tokens, int32_t H,
+                                             int32_t d_k, int32_t d_v,
+                                             int32_t segments);
+
+/* kda_prefill of ONE sequence with its chunks cut into `segments` groups
+ * that run at once (chunk-group parallel prefill): the form for a short
+ * prompt whose chunk chain, not the amount of work, sets the time.
+ *
+ * The recurrence carries only the state from chunk to chunk ("Kimi 모델
+ * 분석", section "순환을 GPU에 올리기") and is linear in (S, v), so each
+ * segment g >= 1 runs twice on the same chunk operands: from S = 0 (its local
+ * outputs and final state L_g) and, with v = 0, from S = I (the product
+ * Phi_g of its token transitions and, per token, Phi_t^T q_t).  A scan then
+ * gives the state entering each segment, S_1 = L_0, S_{g+1} = Phi_g S_g +
+ * L_g, and a fix-up adds S_g^T Phi_t^T q_t to the local outputs.  This is the
+ * one-GPU form of what "[논문 리뷰] Kimi K3 Technical Report", section 13,
+ * calls KDA context parallelism.  The result equals kda_prefill's up to
+ * rounding.
+ *
+ * Arguments and layouts are those of kda_prefill with N = 1 (no cu_seqlens),
+ * plus:
+ *   segments   the number of segments, >= 2 (used when every segment has a
+ *              chunk and the 2 * segments - 1 chains of each head fill at
+ *              most half of the SMs), or <= 0 to let the library choose: the
+ *              most segments for which those chains fill about a third of
+ *              the SMs and every segment has at least 24 chunks (one GB300:
+ *              2 at H = 16, 3 at H = 8, 6 at H = 4; none at H >= 24 or below
+ *              3,072 tokens, where cutting does not pay).
+ *   workspace  kda_prefill_segmented_workspace_bytes(...) bytes, 256-byte
+ *              aligned, not shared with concurrent calls.
+ * When the shape cannot be cut (not bf16 inputs with d_k = d_v = 128, too
+ * many heads for two segments, a single chunk) or the workspace is smaller
+ * than that size, the call is kda_prefill, with the same results.  The
+ * device-side status words are those of kda_prefill (workspace bytes 4 and
+ * 8).  Launches: the work list, the cut prefill, the scan and the fix-up. */
+kda_status_t kda_prefill_segmented(const void *q, const void *k, const void *v,
+                                   const float *log_alpha, const float *beta,
+                                   const float *S0, int64_t total_tokens,
+                                   int32_t H, int32_t d_k, int32_t d_v,
+                                   kda_dtype_t dtype, void *o, float *S_final,
+                                   int32_t segments, void *workspace,
+                                   size_t workspace_bytes, cudaStream_t stream);
+
 /* Device staging bytes kda_prefill_host needs for segments of
  * segment_tokens tokens (a multiple of 64): two input and two output segment
  * buffers, two state buffers and a prefill workspace.  0 for bad arguments. */
