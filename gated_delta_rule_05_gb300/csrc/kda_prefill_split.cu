@@ -572,9 +572,11 @@ __device__ __forceinline__ void producer(const Ctx& X, uint32_t tmem, int warp, 
             const float* sG = reinterpret_cast<const float*>(sm + OFF_G);
             const float* Ah = reinterpret_cast<const float*>(sm + OFF_AH);
             const int npass = gate_prep<FUSED>(X, t, len, sG, Ah, Gq, pp);
-            bool alive = true;
-            for (int p = 0; p < npass; ++p) {
-                const Pass ps = select_pass(pp, p, npass, len);
+            // One pass of the job's front phases into step block p of the
+            // slot.  (Two call sites rather than a loop over the passes, so
+            // that the running sums are not live through the first pass's
+            // solve: a second pass reloads them from the g tile.)
+            auto run_pass = [&](int p, const Pass& ps, const float2 (&Gp)[16]) -> bool {
                 uint8_t* blk = slot + (size_t)p * kStage;
                 if (ct == 0) {
                     X.desc[step & 1].last_step = 0;
@@ -582,7 +584,7 @@ __device__ __forceinline__ void producer(const Ctx& X, uint32_t tmem, int warp, 
                 }
                 group_sync();
                 pass_factors(X, t, ps, reinterpret_cast<float*>(sm + OFF_GL));
-                gram_operands<FUSED, sizeof(TO) == 4>(X, t, ps, Gq, sm + OFF_QG, sm + OFF_KT, sm + P_GK);
+                gram_operands<FUSED, sizeof(TO) == 4>(X, t, ps, Gp, sm + OFF_QG, sm + OFF_KT, sm + P_GK);
                 fence_proxy_async_smem();
                 group_sync();
                 if (ct == 0) {
@@ -617,7 +619,7 @@ __device__ __forceinline__ void producer(const Ctx& X, uint32_t tmem, int warp, 
                         atomicExch(&X.misc->abort, 1);   // the group stops at its next wait
                     }
                 }
-                if (!gram_readout(X, t, tmem, ps.lo, ps.hi, step, sm + OFF_P)) { alive = false; break; }
+                if (!gram_readout(X, t, tmem, ps.lo, ps.hi, step, sm + OFF_P)) return false;
                 if (ct == 0) {
                     bulk_store(blk + BLK_P, sm + OFF_P, 8192);
                     bulk_commit_group();
@@ -627,12 +629,22 @@ __device__ __forceinline__ void producer(const Ctx& X, uint32_t tmem, int warp, 
                     bulk_store(blk + BLK_T16, sm + OFF_T16, 8192);
                     bulk_commit_group();
                 }
-                if (!w_readout(X, t, tmem, step, sm + OFF_WT)) { alive = false; break; }
+                if (!w_readout(X, t, tmem, step, sm + OFF_WT)) return false;
                 if (ct == 0) {
                     bulk_store(blk + BLK_WT, sm + OFF_WT, 16384);
                     bulk_commit_group();
                 }
                 ++step;
+                return true;
+            };
+            const Pass ps0 = select_pass(pp, 0, npass, len);
+            const Pass ps1 = select_pass(pp, 1, npass, len);
+            if (npass == 2) stash_running_sums(t, const_cast<float*>(sG), Gq);
+            bool alive = run_pass(0, ps0, Gq);
+            if (alive && npass == 2) {
+                float2 G2[16];
+                load_running_sums(t, sG, G2);
+                alive = run_pass(1, ps1, G2);
             }
             if (!alive) break;
             prev_npass = npass;

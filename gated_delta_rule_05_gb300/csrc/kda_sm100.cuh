@@ -104,6 +104,14 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads)
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Arrives on a named barrier without waiting (the producer side of a bar.sync
+// with the same id and count); writes before it are visible to the threads
+// that complete the bar.sync.
+__device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t nthreads)
+{
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 // Named barrier that also ORs a predicate over the participating threads.
 __device__ __forceinline__ bool named_bar_red_or(uint32_t id, uint32_t nthreads, bool pred)
 {

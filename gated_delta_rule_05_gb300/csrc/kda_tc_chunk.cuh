@@ -64,6 +64,8 @@ constexpr int kC = 64;
 constexpr int kD = 128;
 constexpr int kGroup = 256;            // compute group: 8 warps
 constexpr int kGroupBar = 1;           // its named barrier
+// Named barriers of the UT solve's warp chains (ids 2 .. 4), see ut_solve.
+constexpr int kBarSolve0 = 2;
 constexpr float kLog2e = 1.4426950408889634f;
 // Largest decay span (log2 units) handled in one pass.
 constexpr float kSpanMax = 250.f;
@@ -80,8 +82,8 @@ constexpr uint32_t OFF_KC = 147456;    // Gram B operand Kc tf32, K-major [64][1
 // After the Gram product, in the operand region [OFF_A, OFF_QG):
 constexpr uint32_t OFF_A32 = OFF_A;           // A fp32 [64][LDA]
 constexpr uint32_t OFF_X = OFF_A + 17408;     // X = (I + A)^-1 fp32 [64][LDA]
-constexpr uint32_t OFF_ZS = OFF_X + 17408;    // solve scratch, 3 x [16][16] fp32
-constexpr uint32_t OFF_STAT = OFF_ZS + 3072;  // gate prep: decay stats fp32 [3][4][128]
+constexpr uint32_t OFF_ZS = OFF_X + 17408;    // solve scratch, 6 x [16][LDZ] fp32 (one per chain);
+constexpr uint32_t OFF_STAT = OFF_ZS;         //   before it, the gate prep's decay stats [3][4][128]
 constexpr uint32_t OFF_T16 = 126976;   // T       [r][i] fp16 (W and V products)
 constexpr uint32_t OFF_WT = 163840;    // -W^T    [ch][r] fp16 (directly before (e^G Q)^T)
 constexpr uint32_t OFF_QG = 180224;    // (e^G Q)^T [ch][r] fp16
@@ -100,7 +102,9 @@ constexpr uint32_t OFF_MISC = 224544;  // tmem base, flags
 constexpr uint32_t kSmemUsed = 224560;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;   // + alignment slack
 constexpr int LDA = 68;                // row stride (floats) of A / X: 16-byte aligned rows
-static_assert(OFF_STAT + 6144 <= OFF_T16 && OFF_T16 + 8192 <= OFF_WT, "post-Gram tiles overlap");
+constexpr int LDZ = 20;                // row stride (floats) of a chain's scratch block
+static_assert(OFF_STAT + 6144 <= OFF_T16 && OFF_ZS + 6 * 16 * LDZ * 4 <= OFF_T16 &&
+              OFF_T16 + 8192 <= OFF_WT, "post-Gram tiles overlap");
 static_assert(OFF_KC + 32768 == OFF_QG && OFF_A + 65536 == OFF_KC, "operand region");
 static_assert(OFF_QG - OFF_WT == 16384 && OFF_KT - OFF_P == 8192,
               "the back products read -W^T | (e^G Q)^T and P | Ktil^T as one tile each");
@@ -405,6 +409,27 @@ __device__ __forceinline__ Pass select_pass(const PassParams& pp, int p, int npa
     return s;
 }
 
+// A chunk of two passes: the threads whose rows fall in the second pass
+// (rq >= 2) keep their running sums in the g tile, in place of the g values
+// they were computed from (each thread writes only what it read), so that
+// they need not stay in registers through the first pass.  The second half
+// of the g tile is not overwritten before the second pass.
+__device__ __forceinline__ void stash_running_sums(const Lane& t, float* sG, const float2 (&Gq)[16])
+{
+    if (t.rq < 2) return;
+#pragma unroll
+    for (int rr = 0; rr < 16; ++rr)
+        *reinterpret_cast<float2*>(sG + (16 * t.rq + rr) * kD + 2 * t.cp) = Gq[rr];
+}
+
+__device__ __forceinline__ void load_running_sums(const Lane& t, const float* sG, float2 (&Gq)[16])
+{
+    const int rq = t.rq < 2 ? t.rq + 2 : t.rq;      // rows of the first pass: unused values
+#pragma unroll
+    for (int rr = 0; rr < 16; ++rr)
+        Gq[rr] = *reinterpret_cast<const float2*>(sG + (16 * rq + rr) * kD + 2 * t.cp);
+}
+
 // Front phase 2: this pass's per-channel e^{G_last} (to gl_dst) and the
 // masked beta.  No barrier.
 __device__ __forceinline__ void pass_factors(const Ctx& X, const Lane& t, const Pass& ps,
@@ -572,26 +597,44 @@ __device__ __forceinline__ bool gram_readout(const Ctx& X, const Lane& t, uint32
     return true;
 }
 
-// Sum over m < 16 of row[m] col[m] (row: 16 floats, 16-byte aligned).
-__device__ __forceinline__ float dot16(const float* row, const float (&col)[16])
+// One warp's 16 x 16 block product acc += L R on the CUDA cores, register-
+// tiled: lane (rp, cq) = (lane / 4, lane % 4) holds rows 2rp, 2rp+1 and
+// columns 4cq .. 4cq+3 of the result, so each 16-byte load feeds eight FMAs
+// (24 loads for 128 FMAs).  L and R are fp32 blocks with 16-byte aligned rows,
+// row strides ldl and ldr (floats).  K runs in two halves of 8: each half's
+// twelve loads are issued together before its FMAs (the chains of the solve
+// are latency-bound), and the halves are a loop, not unrolled, so that the
+// solve's code stays small.
+__device__ __forceinline__ void blk_fma(const float* L, int ldl, const float* R, int ldr, int lane,
+                                        float (&acc)[2][4])
 {
-    float a0 = 0.f, a1 = 0.f;
+    const int rp = lane >> 2, cq = lane & 3;
+    const float* l0 = L + (2 * rp) * ldl;
+    const float* l1 = l0 + ldl;
+    const float* rc = R + 4 * cq;
+#pragma unroll 1
+    for (int k8 = 0; k8 < 16; k8 += 8) {
+        float4 a[2][2], b[8];
 #pragma unroll
-    for (int m4 = 0; m4 < 4; ++m4) {
-        const float4 rv = *reinterpret_cast<const float4*>(row + 4 * m4);
-        a0 = fmaf(rv.x, col[4 * m4 + 0], a0);
-        a1 = fmaf(rv.y, col[4 * m4 + 1], a1);
-        a0 = fmaf(rv.z, col[4 * m4 + 2], a0);
-        a1 = fmaf(rv.w, col[4 * m4 + 3], a1);
+        for (int h = 0; h < 2; ++h) {
+            a[0][h] = *reinterpret_cast<const float4*>(l0 + k8 + 4 * h);
+            a[1][h] = *reinterpret_cast<const float4*>(l1 + k8 + 4 * h);
+        }
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) b[kk] = *reinterpret_cast<const float4*>(rc + (k8 + kk) * ldr);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const float4 av = a[r][kk >> 2];
+                const float x = (kk & 3) == 0 ? av.x : (kk & 3) == 1 ? av.y : (kk & 3) == 2 ? av.z : av.w;
+                acc[r][0] = fmaf(x, b[kk].x, acc[r][0]);
+                acc[r][1] = fmaf(x, b[kk].y, acc[r][1]);
+                acc[r][2] = fmaf(x, b[kk].z, acc[r][2]);
+                acc[r][3] = fmaf(x, b[kk].w, acc[r][3]);
+            }
+        }
     }
-    return a0 + a1;
-}
-
-// A column of 16 floats, stride ld.
-__device__ __forceinline__ void load_col16(const float* p, int ld, float (&col)[16])
-{
-#pragma unroll
-    for (int m = 0; m < 16; ++m) col[m] = p[m * ld];
 }
 
 // Front phase 5: the UT solve, fp32 on the CUDA cores.  From A (OFF_A32)
@@ -599,25 +642,24 @@ __device__ __forceinline__ void load_col16(const float* p, int ld, float (&col)[
 // the fp16 tile t16_dst ([r][i], zero above the diagonal; b = the masked beta
 // of the pass, so T is zero outside the pass).  Arrives B_T at the end.
 //
-// The block recurrence X_ij = -X_ii sum_{j<=k<i} A_ik X_kj runs in rounds;
-// thread (r, c) = (ct / 16, ct % 16) forms element (r, c) of every block
-// product of a round (Z and P: partial sums, Y: finished off-diagonal blocks):
-//   D   X_00 .. X_33 (64 threads, one column of one diagonal block each)
-//   1   Z10 = A10 X00   P20 = A20 X00   P30 = A30 X00   Z21 = A21 X11
-//       P31 = A31 X11   Z32 = A32 X22
-//   2   Y10 = -X11 Z10  Y21 = -X22 Z21  Y32 = -X33 Z32
-//   3   Z20 = P20 + A21 Y10   Z31 = P31 + A32 Y21   P30 += A31 Y10
-//   4   Y20 = -X22 Z20  Y31 = -X33 Z31
-//   5   Z30 = P30 + A32 Y20
-//   6   Y30 = -X33 Z30
-// P stays in the thread's registers; Z goes through OFF_ZS.
+// The diagonal blocks' inverses X_bb come first (64 threads, one column of
+// one block each, by forward substitution).  Then X_ij = -X_ii sum_{j<=k<i}
+// A_ik X_kj for the six blocks below the diagonal, one warp per block, each a
+// chain of register-tiled 16 x 16 products (blk_fma):
+//   (1,0) (2,0) (3,0) (2,1) (3,1) (3,2)
+// A chain needs the blocks X_kj (j < k < i) of the chains before it: Y10 for
+// (2,0) and (3,0), Y20 for (3,0), Y21 for (3,1); the chain that stores such a
+// block arrives on its named barrier and the chains that read it wait there.
+// The sum goes through the warp's scratch block (OFF_ZS) before the last
+// product with X_ii.  (One element per thread for every product instead reads
+// a whole row and column per 16 FMAs: 4.7K cycles per chunk, bound by shared-
+// memory bandwidth.)
 __device__ __forceinline__ void ut_solve(const Ctx& X, const Lane& t, uint8_t* t16_dst)
 {
     uint8_t* sm = X.sm;
     const float* sBst = reinterpret_cast<const float*>(sm + OFF_BST);
     const float* sA = reinterpret_cast<const float*>(sm + OFF_A32);
     float* sX = reinterpret_cast<float*>(sm + OFF_X);
-    float* sZ = reinterpret_cast<float*>(sm + OFF_ZS);
     const int ct = t.ct;
     if (ct < 64) {
         // Column j of the unit-lower diagonal block b, by forward substitution.
@@ -635,60 +677,49 @@ __device__ __forceinline__ void ut_solve(const Ctx& X, const Lane& t, uint8_t* t
         for (int r = 0; r < 16; ++r) xo[r * LDA] = x[r];
     }
     group_sync();
-    const int r = ct >> 4, c = ct & 15;
-    auto arow = [&](int bi, int bj) { return sA + (16 * bi + r) * LDA + 16 * bj; };
-    auto xrow = [&](int bi, int bj) { return sX + (16 * bi + r) * LDA + 16 * bj; };
-    auto xat = [&](int bi, int bj) -> float& { return sX[(16 * bi + r) * LDA + 16 * bj + c]; };
-    float col[16];
-    float p20, p30, p31;
-    // round 1
-    load_col16(sX + c, LDA, col);                                  // X00[:, c]
-    sZ[0 * 256 + r * 16 + c] = dot16(arow(1, 0), col);
-    p20 = dot16(arow(2, 0), col);
-    p30 = dot16(arow(3, 0), col);
-    load_col16(sX + 16 * LDA + 16 + c, LDA, col);                  // X11[:, c]
-    sZ[1 * 256 + r * 16 + c] = dot16(arow(2, 1), col);
-    p31 = dot16(arow(3, 1), col);
-    load_col16(sX + 32 * LDA + 32 + c, LDA, col);                  // X22[:, c]
-    sZ[2 * 256 + r * 16 + c] = dot16(arow(3, 2), col);
-    group_sync();
-    // round 2
-    {
-        float y[3];
+    const int wc = ct >> 5, lane = ct & 31;
+    if (wc < 6) {
+        // chain wc computes block (bi, bj); barrier ids: (1,0) +0, (2,0) +1, (2,1) +2
+        const int bi = (wc < 3) ? wc + 1 : (wc < 5 ? wc - 1 : 3);
+        const int bj = (wc < 3) ? 0 : (wc < 5 ? 1 : 2);
+        float acc[2][4];
 #pragma unroll
-        for (int k = 0; k < 3; ++k) {
-            load_col16(sZ + k * 256 + c, 16, col);
-            y[k] = -dot16(xrow(k + 1, k + 1), col);
+        for (int a = 0; a < 2; ++a)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) acc[a][c] = 0.f;
+#pragma unroll 1
+        for (int k = bj; k < bi; ++k) {
+            if (k > bj) {
+                // block (k, bj) is another chain's result: (1,0), (2,0) or (2,1)
+                const int id = (bj == 0) ? k - 1 : 2;
+                named_bar_sync(kBarSolve0 + id, id == 0 ? 96 : 64);
+            }
+            blk_fma(sA + (16 * bi) * LDA + 16 * k, LDA, sX + (16 * k) * LDA + 16 * bj, LDA, lane,
+                    acc);
         }
-        xat(1, 0) = y[0];
-        xat(2, 1) = y[1];
-        xat(3, 2) = y[2];
+        // Y = -X_ii Z through the warp's scratch block
+        float* Z = reinterpret_cast<float*>(sm + OFF_ZS) + 16 * LDZ * wc;
+        const int rp = lane >> 2, cq = lane & 3;
+#pragma unroll
+        for (int a = 0; a < 2; ++a)
+            *reinterpret_cast<float4*>(Z + (2 * rp + a) * LDZ + 4 * cq) =
+                make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
+        __syncwarp();
+#pragma unroll
+        for (int a = 0; a < 2; ++a)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) acc[a][c] = 0.f;
+        blk_fma(sX + (16 * bi) * LDA + 16 * bi, LDA, Z, LDZ, lane, acc);
+        float* Y = sX + (16 * bi) * LDA + 16 * bj;
+#pragma unroll
+        for (int a = 0; a < 2; ++a)
+            *reinterpret_cast<float4*>(Y + (2 * rp + a) * LDA + 4 * cq) =
+                make_float4(-acc[a][0], -acc[a][1], -acc[a][2], -acc[a][3]);
+        // (1,0) is read by chains 1 and 2, (2,0) by chain 2, (2,1) by chain 4
+        if (wc == 0) named_bar_arrive(kBarSolve0 + 0, 96);
+        else if (wc == 1) named_bar_arrive(kBarSolve0 + 1, 64);
+        else if (wc == 3) named_bar_arrive(kBarSolve0 + 2, 64);
     }
-    group_sync();
-    // round 3
-    load_col16(sX + 16 * LDA + c, LDA, col);                       // Y10[:, c]
-    const float z20 = p20 + dot16(arow(2, 1), col);
-    p30 += dot16(arow(3, 1), col);
-    load_col16(sX + 32 * LDA + 16 + c, LDA, col);                  // Y21[:, c]
-    const float z31 = p31 + dot16(arow(3, 2), col);
-    sZ[0 * 256 + r * 16 + c] = z20;
-    sZ[1 * 256 + r * 16 + c] = z31;
-    group_sync();
-    // round 4
-    load_col16(sZ + c, 16, col);
-    const float y20 = -dot16(xrow(2, 2), col);
-    load_col16(sZ + 256 + c, 16, col);
-    const float y31 = -dot16(xrow(3, 3), col);
-    xat(2, 0) = y20;
-    xat(3, 1) = y31;
-    group_sync();
-    // round 5
-    load_col16(sX + 32 * LDA + c, LDA, col);                       // Y20[:, c]
-    sZ[2 * 256 + r * 16 + c] = p30 + dot16(arow(3, 2), col);
-    group_sync();
-    // round 6
-    load_col16(sZ + 512 + c, 16, col);
-    xat(3, 0) = -dot16(xrow(3, 3), col);
     group_sync();
     // T = X Diag(b), fp16, zero above the diagonal: 512 chunks of 8, two per thread.
 #pragma unroll
@@ -1012,15 +1043,15 @@ __device__ __forceinline__ void state_copy_f16(const Lane& t, uint32_t tmem, uin
 // S^T <- S^T Diag(e^{G_last}) in place.  No barrier.
 __device__ __forceinline__ void state_scale(const Lane& t, uint32_t tmem, const float* gl)
 {
-#pragma unroll
-    for (int jb = 0; jb < 2; ++jb) {
-        const int c0 = 64 * t.half + 32 * jb;
-        uint32_t r[32];
-        tmem_ld32(tmem + t.lane_base + TM_S + c0, r);
+#pragma unroll 1
+    for (int jb = 0; jb < 4; ++jb) {
+        const int c0 = 64 * t.half + 16 * jb;
+        uint32_t r[16];
+        tmem_ld16(tmem + t.lane_base + TM_S + c0, r);
         tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * gl[c0 + i]);
-        tmem_st32(tmem + t.lane_base + TM_S + c0, r);
+        for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * gl[c0 + i]);
+        tmem_st16(tmem + t.lane_base + TM_S + c0, r);
     }
     tmem_st_wait();
 }
