@@ -566,7 +566,9 @@ def bench_short(args, kda, torch, synth, peaks, stream, dev, rank, world, smi_id
     ws = torch.zeros(kda.kda_prefill_workspace_bytes(1, H, d, d), dtype=torch.uint8, device=dev)
     kernel = prefill_kernel_name(ws.numel(), 1)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    ws_seg = torch.zeros(kda.kda_prefill_segmented_workspace_bytes(T, H, d, d, 0),
+    # the segmented call cuts this prompt in two (an explicit count: the
+    # library's own choice leaves a 64-chunk chain uncut)
+    ws_seg = torch.zeros(kda.kda_prefill_segmented_workspace_bytes(T, H, d, d, 2),
                          dtype=torch.uint8, device=dev)
 
     def run():
@@ -575,7 +577,7 @@ def bench_short(args, kda, torch, synth, peaks, stream, dev, rank, world, smi_id
 
     def run_segmented():
         kda.kda_prefill_segmented(sin.q, sin.k, sin.v, sin.log_alpha, sin.beta, S0=None,
-                                  segments=0, o=o, S_final=Sf, workspace=ws_seg, stream=stream)
+                                  segments=2, o=o, S_final=Sf, workspace=ws_seg, stream=stream)
 
     steps = max(args.steps, 20)
 
@@ -602,6 +604,21 @@ def bench_short(args, kda, torch, synth, peaks, stream, dev, rank, world, smi_id
     seg_times, _ = timed(run_segmented, ws_seg)
     ms = sum(times)
     ms_max = max_over_ranks(ms, world, dev)
+    # A prompt of few heads (one tensor-parallel shard of a layer), where the
+    # segmented call pays: 4 heads x 32,768 tokens, the distributions above.
+    fh = synth.generate([32768], 4, d, d, dtype=ws_.dtype, gate=ws_.gate, q_scale=ws_.q_scale,
+                        seed=rank_seed(ws_.seed, rank) + 1, device=dev)
+    fo = torch.empty_like(fh.v)
+    fS = torch.empty((1, 4, d, d), dtype=torch.float32, device=dev)
+    fws = torch.zeros(kda.kda_prefill_workspace_bytes(1, 4, d, d), dtype=torch.uint8, device=dev)
+    fws_seg = torch.zeros(kda.kda_prefill_segmented_workspace_bytes(32768, 4, d, d, 0),
+                          dtype=torch.uint8, device=dev)
+    fh_plain, _ = timed(lambda: kda.kda_prefill(fh.q, fh.k, fh.v, fh.log_alpha, fh.beta, o=fo,
+                                                S_final=fS, workspace=fws, stream=stream), fws)
+    fh_seg, _ = timed(lambda: kda.kda_prefill_segmented(fh.q, fh.k, fh.v, fh.log_alpha, fh.beta,
+                                                        segments=0, o=fo, S_final=fS,
+                                                        workspace=fws_seg, stream=stream), fws_seg)
+    del fh, fo, fS, fws, fws_seg
     alg_bytes = T * H * BYTES_PER_TOKEN_HEAD + H * state_bytes(d)       # + the S_final write
     achieved = alg_bytes / (ms / steps / 1e3) / 1e9
     return {
@@ -614,16 +631,22 @@ def bench_short(args, kda, torch, synth, peaks, stream, dev, rank, world, smi_id
                      "traffic": None, "peak_source": peaks["source"], "kernel": kernel,
                      "algorithmic_bytes_per_launch": alg_bytes},
         # per call: the work-list kernel + the tensor-core kernel; the
-        # segmented call adds the scan and the fix-up
-        "gpu_launches": 2 * steps + 4 * steps,
+        # segmented call adds the scan and the fix-up; both again for the
+        # few-heads prompt
+        "gpu_launches": 2 * (2 * steps + 4 * steps),
         "clocks": clk.summary(),
-        # the same prompt through kda_prefill_segmented (chunk-group parallel
-        # prefill, segments chosen by the library; same results)
-        "segmented": {"ms_per_step": sum(seg_times) / steps,
+        # the same prompt through kda_prefill_segmented in two segments
+        # (chunk-group parallel prefill; same results), and a few-heads prompt
+        # with the segment count chosen by the library (6 at 4 heads)
+        "segmented": {"segments": 2, "ms_per_step": sum(seg_times) / steps,
                       "ms_median": seg_times[len(seg_times) // 2],
                       "tokens_per_s": T * steps / (sum(seg_times) / 1e3),
                       "speedup_vs_kda_prefill": sum(times) / sum(seg_times),
-                      "workspace_bytes": int(ws_seg.numel())},
+                      "workspace_bytes": int(ws_seg.numel()),
+                      "few_heads_h4_t32768": {
+                          "kda_prefill_ms": sum(fh_plain) / steps,
+                          "segmented_ms": sum(fh_seg) / steps,
+                          "speedup_vs_kda_prefill": sum(fh_plain) / sum(fh_seg)}},
     }
 
 

@@ -61,8 +61,14 @@ def check(kda, inp, segments, o_dtype=None):
 
 
 def test_prefill_h16_t4096_segmented(kda):
-    # the short-prompt workload: 16 heads, 64 chunks; two segments by default
+    # the short-prompt workload: 16 heads, 64 chunks, in two segments (the
+    # automatic choice leaves it uncut: there it is on par with kda_prefill)
     inp = synth.workload_inputs(2, device="cpu")
+    check(kda, inp, 2)
+
+
+def test_automatic_choice_cuts_a_long_few_head_prompt(kda):
+    inp = synth.generate([16384], 4, 128, 128, dtype="bf16", s0_std=0.05, seed=715)
     check(kda, inp, 0)
 
 
