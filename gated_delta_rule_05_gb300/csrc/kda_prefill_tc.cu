@@ -282,7 +282,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 tc_fence_before();
 
                 if (!gram_readout(X, t, tmem, ps.lo, ps.hi, step, sm + OFF_P)) { alive = false; break; }
-                ut_solve(X, t, sm + OFF_T16);
+                ut_solve_mma(X, t, sm + OFF_T16);
                 if (!w_readout(X, t, tmem, step, sm + OFF_WT)) { alive = false; break; }
                 if (ct == 0) {
                     // The W product has read the (e^G K)^T tile: after the

@@ -82,7 +82,7 @@ constexpr uint32_t OFF_KC = 147456;    // Gram B operand Kc tf32, K-major [64][1
 // After the Gram product, in the operand region [OFF_A, OFF_QG):
 constexpr uint32_t OFF_A32 = OFF_A;           // A fp32 [64][LDA]
 constexpr uint32_t OFF_X = OFF_A + 17408;     // X = (I + A)^-1 fp32 [64][LDA]
-constexpr uint32_t OFF_ZS = OFF_X + 17408;    // solve scratch, 6 x [16][LDZ] fp32 (one per chain);
+constexpr uint32_t OFF_ZS = OFF_X + 17408;    // solve scratch, 6 x [16][LDZ] (or [16][LDT]) fp32;
 constexpr uint32_t OFF_STAT = OFF_ZS;         //   before it, the gate prep's decay stats [3][4][128]
 constexpr uint32_t OFF_T16 = 126976;   // T       [r][i] fp16 (W and V products)
 constexpr uint32_t OFF_WT = 163840;    // -W^T    [ch][r] fp16 (directly before (e^G Q)^T)
@@ -104,6 +104,7 @@ constexpr uint32_t kSmemBytes = kSmemUsed + 1024;   // + alignment slack
 constexpr int LDA = 68;                // row stride (floats) of A / X: 16-byte aligned rows
 constexpr int LDZ = 20;                // row stride (floats) of a chain's scratch block
 static_assert(OFF_STAT + 6144 <= OFF_T16 && OFF_ZS + 6 * 16 * LDZ * 4 <= OFF_T16 &&
+              OFF_ZS + 6 * 16 * 24 * 4 <= OFF_T16 &&
               OFF_T16 + 8192 <= OFF_WT, "post-Gram tiles overlap");
 static_assert(OFF_KC + 32768 == OFF_QG && OFF_A + 65536 == OFF_KC, "operand region");
 static_assert(OFF_QG - OFF_WT == 16384 && OFF_KT - OFF_P == 8192,
@@ -719,6 +720,204 @@ __device__ __forceinline__ void ut_solve(const Ctx& X, const Lane& t, uint8_t* t
         if (wc == 0) named_bar_arrive(kBarSolve0 + 0, 96);
         else if (wc == 1) named_bar_arrive(kBarSolve0 + 1, 64);
         else if (wc == 3) named_bar_arrive(kBarSolve0 + 2, 64);
+    }
+    group_sync();
+    // T = X Diag(b), fp16, zero above the diagonal: 512 chunks of 8, two per thread.
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+        const int q = ct + 256 * e, rr = q >> 3, j = q & 7;
+        const float4* xr = reinterpret_cast<const float4*>(sX + rr * LDA + 8 * j);
+        const float4* bb = reinterpret_cast<const float4*>(sBst + 8 * j);
+        const float4 x0 = xr[0], x1 = xr[1], b0 = bb[0], b1 = bb[1];
+        const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+        const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+        uint32_t pk[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int i0 = 8 * j + 2 * k;
+            pk[k] = pack_f16x2(i0 <= rr ? xv[2 * k] * bv[2 * k] : 0.f,
+                               i0 + 1 <= rr ? xv[2 * k + 1] * bv[2 * k + 1] : 0.f);
+        }
+        st_chunk(t16_dst, rr, j, make_uint4(pk[0], pk[1], pk[2], pk[3]));
+    }
+    fence_proxy_async_smem();      // T is read by the W product (and copied out)
+    group_sync();
+    if (ct == 0) mbar_arrive(&X.bar[B_T]);
+}
+
+// ---- the UT solve's 16 x 16 block products on the warp tensor cores.
+// Operands are fp32 values split into fp16 pairs x = hi + lo (hi = x rounded
+// to fp16, lo = the rest rounded to fp16); a product takes the three terms
+// hi hi + hi lo + lo hi with fp32 accumulation: about 22 significant bits
+// (entries below 2^-3 keep an absolute accuracy of about 2^-25, from lo's
+// subnormals).  X's entries must stay below 65504 (T = X Diag(beta) is fp16
+// anyway).  A bf16 split (16 bits, fp32's range) lost too much where the
+// chain products cancel: beta = 2 with no decay moved o by 4 % of its RMS.
+
+// Splits (x0, x1) into packed fp16 pairs: hi and lo.
+__device__ __forceinline__ void split_f16x2(float x0, float x1, uint32_t& hi, uint32_t& lo)
+{
+    hi = pack_f16x2(x0, x1);
+    const float2 h = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+    lo = pack_f16x2(x0 - h.x, x1 - h.y);
+}
+
+// d += a b for one m16n8k16 tile (a: 4 registers, b: 2, d: 4).
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                              uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// c[nh] += L R for a 16 x 16 output in two 16 x 8 halves, three terms each.
+// The A fragment is given split (ah, al); the B fragment of half nh is read
+// from row-major fp32 storage where element (k, n) of B sits at
+// bsrc[n * ldb + k] (so B^T is stored row-major), for the lane's rows g and
+// g + 8 of each half and columns 2 tq, 2 tq + 1 and 2 tq + 8, 2 tq + 9.
+__device__ __forceinline__ void blk_mma(float (&c)[2][4], const uint32_t (&ah)[4],
+                                        const uint32_t (&al)[4], const float* bsrc, int ldb,
+                                        int g, int tq)
+{
+#pragma unroll
+    for (int nh = 0; nh < 2; ++nh) {
+        const float* br = bsrc + (8 * nh + g) * ldb + 2 * tq;
+        const float2 x0 = *reinterpret_cast<const float2*>(br);
+        const float2 x1 = *reinterpret_cast<const float2*>(br + 8);
+        uint32_t bh0, bl0, bh1, bl1;
+        split_f16x2(x0.x, x0.y, bh0, bl0);
+        split_f16x2(x1.x, x1.y, bh1, bl1);
+        mma_f16_16816(c[nh], ah, bh0, bh1);
+        mma_f16_16816(c[nh], ah, bl0, bl1);
+        mma_f16_16816(c[nh], al, bh0, bh1);
+    }
+}
+
+// Transposed copies of the blocks that later chains read as A operands:
+// X00, X11, X22 and Y10, Y20, Y21, [16][LDT] fp32 each, at OFF_ZS.
+constexpr int LDT = 24;                // row stride (floats): conflict-free 8-byte fragment loads
+__device__ __forceinline__ int xt_slot(int k, int j)
+{
+    return (k == j) ? k : (k == 1 ? 3 : (j == 0 ? 4 : 5));
+}
+
+// Front phase 5 as the single-CTA kernel runs it: the UT solve with its block
+// products on the warp tensor cores.  From A (OFF_A32) builds X = (I + A)^{-1}
+// (OFF_X) block by block and writes T = X Diag(b) as the fp16 tile t16_dst
+// ([r][i], zero above the diagonal; b = the masked beta of the pass, so T is
+// zero outside the pass).  Arrives B_T at the end.
+//
+// The diagonal blocks' inverses X_bb come first (64 threads, one column of
+// one block each, by forward substitution, in fp32).  Then X_ij = -X_ii
+// sum_{j<=k<i} A_ik X_kj for the six blocks below the diagonal, one warp per
+// block, as chains of 16 x 16 products on the warp tensor cores (blk_mma):
+//   (1,0) (2,0) (3,0) (2,1) (3,1) (3,2)
+// Each chain works on transposes, Z^T = sum X_kj^T A_ik^T and X_ij^T =
+// -Z^T X_ii^T, so that the first product's accumulators are already the A
+// fragment of the second.  A chain needs the blocks X_kj (j < k < i) of the
+// chains before it: Y10 for (2,0) and (3,0), Y20 for (3,0), Y21 for (3,1);
+// the chain that stores such a block arrives on its named barrier and the
+// chains that read it wait there.  (With fp32 FMAs on the CUDA cores, the
+// chains' critical path of six products took about 3.3K cycles per chunk.)
+__device__ __forceinline__ void ut_solve_mma(const Ctx& X, const Lane& t, uint8_t* t16_dst)
+{
+    uint8_t* sm = X.sm;
+    const float* sBst = reinterpret_cast<const float*>(sm + OFF_BST);
+    const float* sA = reinterpret_cast<const float*>(sm + OFF_A32);
+    float* sX = reinterpret_cast<float*>(sm + OFF_X);
+    float* sXt = reinterpret_cast<float*>(sm + OFF_ZS);
+    const int ct = t.ct;
+    if (ct < 64) {
+        // Column j of the unit-lower diagonal block b, by forward substitution.
+        const int b = ct >> 4, j = ct & 15;
+        const float* L = sA + (16 * b) * LDA + 16 * b;
+        float x[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) x[r] = (r == j) ? 1.f : 0.f;
+#pragma unroll
+        for (int i = 0; i < 15; ++i)
+#pragma unroll
+            for (int r = i + 1; r < 16; ++r) x[r] = fmaf(-L[r * LDA + i], x[i], x[r]);
+        float* xo = sX + (16 * b) * LDA + 16 * b + j;
+#pragma unroll
+        for (int r = 0; r < 16; ++r) xo[r * LDA] = x[r];
+        if (b < 3) {   // the transposed copy: column j of X_bb is row j of X_bb^T
+            float4* xt = reinterpret_cast<float4*>(sXt + xt_slot(b, b) * 16 * LDT + j * LDT);
+#pragma unroll
+            for (int r4 = 0; r4 < 4; ++r4)
+                xt[r4] = make_float4(x[4 * r4], x[4 * r4 + 1], x[4 * r4 + 2], x[4 * r4 + 3]);
+        }
+    }
+    group_sync();
+    const int wc = ct >> 5, lane = ct & 31;
+    if (wc < 6) {
+        // chain wc computes block (bi, bj); barrier ids: (1,0) +0, (2,0) +1, (2,1) +2
+        const int bi = (wc < 3) ? wc + 1 : (wc < 5 ? wc - 1 : 3);
+        const int bj = (wc < 3) ? 0 : (wc < 5 ? 1 : 2);
+        const int g = lane >> 2, tq = lane & 3;
+        float c[2][4];
+#pragma unroll
+        for (int nh = 0; nh < 2; ++nh)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) c[nh][e] = 0.f;
+#pragma unroll 1
+        for (int k = bj; k < bi; ++k) {
+            if (k > bj) {
+                // block (k, bj) is another chain's result: (1,0), (2,0) or (2,1)
+                const int id = (bj == 0) ? k - 1 : 2;
+                named_bar_sync(kBarSolve0 + id, id == 0 ? 96 : 64);
+            }
+            // A fragment: X_kj^T (rows of the transposed copy).
+            const float* xt = sXt + xt_slot(k, bj) * 16 * LDT + 2 * tq;
+            const float2 a0 = *reinterpret_cast<const float2*>(xt + g * LDT);
+            const float2 a1 = *reinterpret_cast<const float2*>(xt + (g + 8) * LDT);
+            const float2 a2 = *reinterpret_cast<const float2*>(xt + g * LDT + 8);
+            const float2 a3 = *reinterpret_cast<const float2*>(xt + (g + 8) * LDT + 8);
+            uint32_t ah[4], al[4];
+            split_f16x2(a0.x, a0.y, ah[0], al[0]);
+            split_f16x2(a1.x, a1.y, ah[1], al[1]);
+            split_f16x2(a2.x, a2.y, ah[2], al[2]);
+            split_f16x2(a3.x, a3.y, ah[3], al[3]);
+            // B = A_ik^T: element (k', n) = A_ik[n][k'], rows of A.
+            blk_mma(c, ah, al, sA + (16 * bi) * LDA + 16 * k, LDA, g, tq);
+        }
+        // Y^T = Z^T X_ii^T: the accumulators are the A fragment; B = X_ii^T,
+        // element (k', n) = X_ii[n][k'], rows of X_ii.
+        uint32_t ah[4], al[4];
+        split_f16x2(c[0][0], c[0][1], ah[0], al[0]);
+        split_f16x2(c[0][2], c[0][3], ah[1], al[1]);
+        split_f16x2(c[1][0], c[1][1], ah[2], al[2]);
+        split_f16x2(c[1][2], c[1][3], ah[3], al[3]);
+        float y[2][4];
+#pragma unroll
+        for (int nh = 0; nh < 2; ++nh)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) y[nh][e] = 0.f;
+        blk_mma(y, ah, al, sX + (16 * bi) * LDA + 16 * bi, LDA, g, tq);
+        // X_ij = -Y: element (m, n) of Y^T is X_ij[n][m] with m = g, g + 8 and
+        // n = 8 nh + 2 tq, 8 nh + 2 tq + 1.
+        float* xo = sX + (16 * bi) * LDA + 16 * bj;
+#pragma unroll
+        for (int nh = 0; nh < 2; ++nh)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int m = g + 8 * (e >> 1), n = 8 * nh + 2 * tq + (e & 1);
+                xo[n * LDA + m] = -y[nh][e];
+            }
+        if (wc == 0 || wc == 1 || wc == 3) {
+            // (1,0) is read by chains 1 and 2, (2,0) by chain 2, (2,1) by chain 4
+            float* xt = sXt + xt_slot(bi, bj) * 16 * LDT + 2 * tq;
+#pragma unroll
+            for (int nh = 0; nh < 2; ++nh) {
+                *reinterpret_cast<float2*>(xt + g * LDT + 8 * nh) = make_float2(-y[nh][0], -y[nh][1]);
+                *reinterpret_cast<float2*>(xt + (g + 8) * LDT + 8 * nh) =
+                    make_float2(-y[nh][2], -y[nh][3]);
+            }
+            named_bar_arrive(kBarSolve0 + (wc == 3 ? 2 : wc), wc == 0 ? 96 : 64);
+        }
     }
     group_sync();
     // T = X Diag(b), fp16, zero above the diagonal: 512 chunks of 8, two per thread.
