@@ -682,7 +682,7 @@ def host_memory_available():
     return avail if avail is not None else 8 << 30
 
 
-E2E_SEGMENT_TOKENS = 16384
+E2E_SEGMENT_TOKENS = 65536
 
 
 def run_e2e(kda, torch, inp, dev, stream, args, world):
