@@ -624,7 +624,7 @@ __device__ __forceinline__ void producer(const Ctx& X, uint32_t tmem, int warp, 
                     bulk_store(blk + BLK_P, sm + OFF_P, 8192);
                     bulk_commit_group();
                 }
-                ut_solve(X, t, sm + OFF_T16);
+                ut_solve_mma(X, t, sm + OFF_T16);
                 if (ct == 0) {
                     bulk_store(blk + BLK_T16, sm + OFF_T16, 8192);
                     bulk_commit_group();

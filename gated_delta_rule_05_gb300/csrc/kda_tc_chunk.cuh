@@ -40,11 +40,11 @@
 // solve runs in fp32 and the state is carried in fp32.  |v| and the state
 // entries are assumed to stay inside the fp16 range (|x| < 65504).
 //
-// UT solve.  X = (I + A)^{-1} by block forward substitution on 16 x 16 blocks,
-// in fp32 on the CUDA cores: the diagonal blocks' inverses X_bb by column-wise
-// substitution, then X_ij = -X_ii sum_{j <= k < i} A_ik X_kj for i > j, in six
-// barrier-separated rounds of 16 x 16 block products that start every product
-// as soon as its factors exist (a lookahead order of the block recurrence).
+// UT solve.  X = (I + A)^{-1} by block forward substitution on 16 x 16 blocks:
+// the diagonal blocks' inverses X_bb in fp32 on the CUDA cores by column-wise
+// substitution, then X_ij = -X_ii sum_{j <= k < i} A_ik X_kj for i > j as six
+// warp chains of 16 x 16 products on the warp tensor cores, each operand split
+// into two fp16 terms (about 22 significant bits, see ut_solve_mma).
 // T = X Diag(b).  W = T (e^G K) is then one tensor-core product with the fp16
 // T and (e^G K)^T tiles.
 
@@ -64,7 +64,7 @@ constexpr int kC = 64;
 constexpr int kD = 128;
 constexpr int kGroup = 256;            // compute group: 8 warps
 constexpr int kGroupBar = 1;           // its named barrier
-// Named barriers of the UT solve's warp chains (ids 2 .. 4), see ut_solve.
+// Named barriers of the UT solve's warp chains (ids 2 .. 4), see ut_solve_mma.
 constexpr int kBarSolve0 = 2;
 constexpr float kLog2e = 1.4426950408889634f;
 // Largest decay span (log2 units) handled in one pass.
@@ -598,153 +598,6 @@ __device__ __forceinline__ bool gram_readout(const Ctx& X, const Lane& t, uint32
     return true;
 }
 
-// One warp's 16 x 16 block product acc += L R on the CUDA cores, register-
-// tiled: lane (rp, cq) = (lane / 4, lane % 4) holds rows 2rp, 2rp+1 and
-// columns 4cq .. 4cq+3 of the result, so each 16-byte load feeds eight FMAs
-// (24 loads for 128 FMAs).  L and R are fp32 blocks with 16-byte aligned rows,
-// row strides ldl and ldr (floats).  K runs in two halves of 8: each half's
-// twelve loads are issued together before its FMAs (the chains of the solve
-// are latency-bound), and the halves are a loop, not unrolled, so that the
-// solve's code stays small.
-__device__ __forceinline__ void blk_fma(const float* L, int ldl, const float* R, int ldr, int lane,
-                                        float (&acc)[2][4])
-{
-    const int rp = lane >> 2, cq = lane & 3;
-    const float* l0 = L + (2 * rp) * ldl;
-    const float* l1 = l0 + ldl;
-    const float* rc = R + 4 * cq;
-#pragma unroll 1
-    for (int k8 = 0; k8 < 16; k8 += 8) {
-        float4 a[2][2], b[8];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            a[0][h] = *reinterpret_cast<const float4*>(l0 + k8 + 4 * h);
-            a[1][h] = *reinterpret_cast<const float4*>(l1 + k8 + 4 * h);
-        }
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) b[kk] = *reinterpret_cast<const float4*>(rc + (k8 + kk) * ldr);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                const float4 av = a[r][kk >> 2];
-                const float x = (kk & 3) == 0 ? av.x : (kk & 3) == 1 ? av.y : (kk & 3) == 2 ? av.z : av.w;
-                acc[r][0] = fmaf(x, b[kk].x, acc[r][0]);
-                acc[r][1] = fmaf(x, b[kk].y, acc[r][1]);
-                acc[r][2] = fmaf(x, b[kk].z, acc[r][2]);
-                acc[r][3] = fmaf(x, b[kk].w, acc[r][3]);
-            }
-        }
-    }
-}
-
-// Front phase 5: the UT solve, fp32 on the CUDA cores.  From A (OFF_A32)
-// builds X = (I + A)^{-1} (OFF_X) block by block and writes T = X Diag(b) as
-// the fp16 tile t16_dst ([r][i], zero above the diagonal; b = the masked beta
-// of the pass, so T is zero outside the pass).  Arrives B_T at the end.
-//
-// The diagonal blocks' inverses X_bb come first (64 threads, one column of
-// one block each, by forward substitution).  Then X_ij = -X_ii sum_{j<=k<i}
-// A_ik X_kj for the six blocks below the diagonal, one warp per block, each a
-// chain of register-tiled 16 x 16 products (blk_fma):
-//   (1,0) (2,0) (3,0) (2,1) (3,1) (3,2)
-// A chain needs the blocks X_kj (j < k < i) of the chains before it: Y10 for
-// (2,0) and (3,0), Y20 for (3,0), Y21 for (3,1); the chain that stores such a
-// block arrives on its named barrier and the chains that read it wait there.
-// The sum goes through the warp's scratch block (OFF_ZS) before the last
-// product with X_ii.  (One element per thread for every product instead reads
-// a whole row and column per 16 FMAs: 4.7K cycles per chunk, bound by shared-
-// memory bandwidth.)
-__device__ __forceinline__ void ut_solve(const Ctx& X, const Lane& t, uint8_t* t16_dst)
-{
-    uint8_t* sm = X.sm;
-    const float* sBst = reinterpret_cast<const float*>(sm + OFF_BST);
-    const float* sA = reinterpret_cast<const float*>(sm + OFF_A32);
-    float* sX = reinterpret_cast<float*>(sm + OFF_X);
-    const int ct = t.ct;
-    if (ct < 64) {
-        // Column j of the unit-lower diagonal block b, by forward substitution.
-        const int b = ct >> 4, j = ct & 15;
-        const float* L = sA + (16 * b) * LDA + 16 * b;
-        float x[16];
-#pragma unroll
-        for (int r = 0; r < 16; ++r) x[r] = (r == j) ? 1.f : 0.f;
-#pragma unroll
-        for (int i = 0; i < 15; ++i)
-#pragma unroll
-            for (int r = i + 1; r < 16; ++r) x[r] = fmaf(-L[r * LDA + i], x[i], x[r]);
-        float* xo = sX + (16 * b) * LDA + 16 * b + j;
-#pragma unroll
-        for (int r = 0; r < 16; ++r) xo[r * LDA] = x[r];
-    }
-    group_sync();
-    const int wc = ct >> 5, lane = ct & 31;
-    if (wc < 6) {
-        // chain wc computes block (bi, bj); barrier ids: (1,0) +0, (2,0) +1, (2,1) +2
-        const int bi = (wc < 3) ? wc + 1 : (wc < 5 ? wc - 1 : 3);
-        const int bj = (wc < 3) ? 0 : (wc < 5 ? 1 : 2);
-        float acc[2][4];
-#pragma unroll
-        for (int a = 0; a < 2; ++a)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) acc[a][c] = 0.f;
-#pragma unroll 1
-        for (int k = bj; k < bi; ++k) {
-            if (k > bj) {
-                // block (k, bj) is another chain's result: (1,0), (2,0) or (2,1)
-                const int id = (bj == 0) ? k - 1 : 2;
-                named_bar_sync(kBarSolve0 + id, id == 0 ? 96 : 64);
-            }
-            blk_fma(sA + (16 * bi) * LDA + 16 * k, LDA, sX + (16 * k) * LDA + 16 * bj, LDA, lane,
-                    acc);
-        }
-        // Y = -X_ii Z through the warp's scratch block
-        float* Z = reinterpret_cast<float*>(sm + OFF_ZS) + 16 * LDZ * wc;
-        const int rp = lane >> 2, cq = lane & 3;
-#pragma unroll
-        for (int a = 0; a < 2; ++a)
-            *reinterpret_cast<float4*>(Z + (2 * rp + a) * LDZ + 4 * cq) =
-                make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
-        __syncwarp();
-#pragma unroll
-        for (int a = 0; a < 2; ++a)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) acc[a][c] = 0.f;
-        blk_fma(sX + (16 * bi) * LDA + 16 * bi, LDA, Z, LDZ, lane, acc);
-        float* Y = sX + (16 * bi) * LDA + 16 * bj;
-#pragma unroll
-        for (int a = 0; a < 2; ++a)
-            *reinterpret_cast<float4*>(Y + (2 * rp + a) * LDA + 4 * cq) =
-                make_float4(-acc[a][0], -acc[a][1], -acc[a][2], -acc[a][3]);
-        // (1,0) is read by chains 1 and 2, (2,0) by chain 2, (2,1) by chain 4
-        if (wc == 0) named_bar_arrive(kBarSolve0 + 0, 96);
-        else if (wc == 1) named_bar_arrive(kBarSolve0 + 1, 64);
-        else if (wc == 3) named_bar_arrive(kBarSolve0 + 2, 64);
-    }
-    group_sync();
-    // T = X Diag(b), fp16, zero above the diagonal: 512 chunks of 8, two per thread.
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-        const int q = ct + 256 * e, rr = q >> 3, j = q & 7;
-        const float4* xr = reinterpret_cast<const float4*>(sX + rr * LDA + 8 * j);
-        const float4* bb = reinterpret_cast<const float4*>(sBst + 8 * j);
-        const float4 x0 = xr[0], x1 = xr[1], b0 = bb[0], b1 = bb[1];
-        const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-        const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-        uint32_t pk[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int i0 = 8 * j + 2 * k;
-            pk[k] = pack_f16x2(i0 <= rr ? xv[2 * k] * bv[2 * k] : 0.f,
-                               i0 + 1 <= rr ? xv[2 * k + 1] * bv[2 * k + 1] : 0.f);
-        }
-        st_chunk(t16_dst, rr, j, make_uint4(pk[0], pk[1], pk[2], pk[3]));
-    }
-    fence_proxy_async_smem();      // T is read by the W product (and copied out)
-    group_sync();
-    if (ct == 0) mbar_arrive(&X.bar[B_T]);
-}
-
 // ---- the UT solve's 16 x 16 block products on the warp tensor cores.
 // Operands are fp32 values split into fp16 pairs x = hi + lo (hi = x rounded
 // to fp16, lo = the rest rounded to fp16); a product takes the three terms
@@ -804,8 +657,8 @@ __device__ __forceinline__ int xt_slot(int k, int j)
     return (k == j) ? k : (k == 1 ? 3 : (j == 0 ? 4 : 5));
 }
 
-// Front phase 5 as the single-CTA kernel runs it: the UT solve with its block
-// products on the warp tensor cores.  From A (OFF_A32) builds X = (I + A)^{-1}
+// Front phase 5: the UT solve with its block products on the warp tensor
+// cores.  From A (OFF_A32) builds X = (I + A)^{-1}
 // (OFF_X) block by block and writes T = X Diag(b) as the fp16 tile t16_dst
 // ([r][i], zero above the diagonal; b = the masked beta of the pass, so T is
 // zero outside the pass).  Arrives B_T at the end.

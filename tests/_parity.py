@@ -103,14 +103,13 @@ def oracle_prefill(inp, heads=None, cols=None, seg_tokens=None, nthreads=None):
 
 def assert_kernels_agree(a, b, what=""):
     """Two prefill kernels on the same call: they evaluate the same products on
-    the same 16-bit operands except for the UT solve's 16 x 16 block products
-    (fp32 FMAs in one, three-term fp16 warp MMAs in the other, both accurate to
-    about 2^-22 before T is rounded to fp16).  Where that tiny difference moves
-    an fp16 rounding of T, o and S move by about 2^-11 of a term, and with no
-    decay (alpha = 1) such moves add up over the whole sequence.  So the two
-    agree to two bf16 ulps of each element (for bf16 outputs) plus 1e-2 of the
-    RMS, half of either's bound against the oracle; a structural fault (a
-    chunk, head or token out of place) moves o by its own size."""
+    the same 16-bit operands.  Any rounding difference between them (a UT
+    solve product accurate to about 2^-22 that moves an fp16 rounding of T)
+    moves o and S by about 2^-11 of a term, and with no decay (alpha = 1) such
+    moves add up over the whole sequence.  So the check allows two bf16 ulps
+    of each element (for bf16 outputs) plus 1e-2 of the RMS, half of either's
+    bound against the oracle; a structural fault (a chunk, head or token out
+    of place) moves o by its own size."""
     x, y = a.double(), b.double()
     rms = y.pow(2).mean().sqrt().item() if y.numel() else 0.0
     bound = torch.full_like(y, 1e-2 * rms)

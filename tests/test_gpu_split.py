@@ -9,10 +9,9 @@ for the same call, so every case here runs both and checks
   * each against the float64 oracle (the bf16 bound of the other parity
     tests, for both kernels), and
   * the two against each other: they evaluate the same products on the same
-    fp16 / bf16 operands in the same order, except for the UT solve's block
-    products (fp32 FMAs on the producers, three-term bf16 warp MMAs on the
-    single-CTA kernel), so o and S_final agree to a couple of bf16 ulps
-    (tests._parity.assert_kernels_agree);
+    fp16 / bf16 operands in the same order (the split kernel only moves the
+    state-independent phases to other CTAs), so o and S_final agree to a
+    couple of bf16 ulps at most (tests._parity.assert_kernels_agree);
   * that the split kernel really ran (its job counter in the workspace) and
     no wait gave up (the timeout word).
 """
