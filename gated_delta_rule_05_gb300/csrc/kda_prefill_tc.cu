@@ -267,22 +267,20 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 group_sync();
                 if (ct == 0) mbar_arrive(&X.bar[B_OPS]);
 
-                // ---- while the Gram runs: the v tile to fp16 (first pass of a
-                // chunk) and the state decay with its fp16 copy.
+                // ---- while the Gram runs: the state decay with its fp16 copy.
+                // (The v tile is converted to fp16 during the UT solve, by the
+                // warps that run no chain: during the Gram its shared-memory
+                // traffic competes with the product's operand reads.)
                 const StepDesc d = X.desc[step & 1];
-                if (d.first_pass) {
-                    if (!group_wait(X, B_V_FULL, chunk_v)) { alive = false; break; }
-                    v_tile_to_f16(sm + OFF_V, ct);
-                }
+                const uint32_t v_phase = (uint32_t)chunk_v;
                 if (d.last_pass) ++chunk_v;
                 tc_fence_after();
                 state_decay(t, tmem, reinterpret_cast<const float*>(sm + OFF_GL),
                             d.first_pass ? snapshot_at(snap, ch, eos - bos, seq_off, H, h) : nullptr);
-                fence_proxy_async_smem();                  // the converted v tile
                 tc_fence_before();
 
                 if (!gram_readout(X, t, tmem, ps.lo, ps.hi, step, sm + OFF_P)) { alive = false; break; }
-                ut_solve_mma(X, t, sm + OFF_T16);
+                ut_solve_mma(X, t, sm + OFF_T16, d.first_pass ? sm + OFF_V : nullptr, v_phase);
                 if (!w_readout(X, t, tmem, step, sm + OFF_WT)) { alive = false; break; }
                 if (ct == 0) {
                     // The W product has read the (e^G K)^T tile: after the

@@ -658,7 +658,8 @@ __device__ __forceinline__ int xt_slot(int k, int j)
 }
 
 // Front phase 5: the UT solve with its block products on the warp tensor
-// cores.  From A (OFF_A32) builds X = (I + A)^{-1}
+// cores.  With a v tile given, the two warps that run no chain convert it to
+// fp16 meanwhile (see the end of the chain phase).  From A (OFF_A32) builds X = (I + A)^{-1}
 // (OFF_X) block by block and writes T = X Diag(b) as the fp16 tile t16_dst
 // ([r][i], zero above the diagonal; b = the masked beta of the pass, so T is
 // zero outside the pass).  Arrives B_T at the end.
@@ -675,7 +676,8 @@ __device__ __forceinline__ int xt_slot(int k, int j)
 // the chain that stores such a block arrives on its named barrier and the
 // chains that read it wait there.  (With fp32 FMAs on the CUDA cores, the
 // chains' critical path of six products took about 3.3K cycles per chunk.)
-__device__ __forceinline__ void ut_solve_mma(const Ctx& X, const Lane& t, uint8_t* t16_dst)
+__device__ __forceinline__ void ut_solve_mma(const Ctx& X, const Lane& t, uint8_t* t16_dst,
+                                             uint8_t* vtile = nullptr, uint32_t v_phase = 0)
 {
     uint8_t* sm = X.sm;
     const float* sBst = reinterpret_cast<const float*>(sm + OFF_BST);
@@ -770,6 +772,22 @@ __device__ __forceinline__ void ut_solve_mma(const Ctx& X, const Lane& t, uint8_
                     make_float2(-y[nh][2], -y[nh][3]);
             }
             named_bar_arrive(kBarSolve0 + (wc == 3 ? 2 : wc), wc == 0 ? 96 : 64);
+        }
+    } else if (vtile != nullptr) {
+        // The two warps without a chain: the chunk's v tile (its TMA load,
+        // phase v_phase of B_V_FULL) from bf16 to fp16 in place, off the
+        // Gram product's shared-memory reads.
+        if (wait_bar(X, B_V_FULL, v_phase)) {
+            uint4* vt = reinterpret_cast<uint4*>(vtile);
+            for (int i = ct - 192; i < 1024; i += 64) {
+                uint4 x = vt[i];
+                x.x = bf16x2_to_f16x2(x.x);
+                x.y = bf16x2_to_f16x2(x.y);
+                x.z = bf16x2_to_f16x2(x.z);
+                x.w = bf16x2_to_f16x2(x.w);
+                vt[i] = x;
+            }
+            fence_proxy_async_smem();
         }
     }
     group_sync();
