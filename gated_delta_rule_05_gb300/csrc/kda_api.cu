@@ -153,12 +153,12 @@ namespace {
 // automatic); 1 means the sequence is not cut.  An explicit request is used
 // when it is possible: every segment non-empty, the consumer units (H (2G - 1))
 // at most half of the SMs.  The automatic choice keeps the units to about a
-// third of the SMs and the segments to at least 48 chunks: more units leave
+// third of the SMs and the segments to at least 32 chunks: more units leave
 // too few producers, shorter segments too little chain to save.  Measured on
-// one GB300 (152 SMs), one sequence, against kda_prefill: H = 16 (2
-// segments) on par at 4,096 tokens, 9 % faster at 8,192 and 14 % at 16,384;
-// H = 8 (3 segments) 2.0x at 65,536; H = 4 (6 segments) 2.8x at 32,768;
-// H = 24 slower, so not cut.
+// one GB300 (152 SMs), one sequence, L2 flushed, the launches' kernel
+// times summed, against kda_prefill: H = 16 (2 segments) 1.19x at 4,096
+// tokens (118 against 140 us) and 1.39x at 16,384; H = 8 (3 segments) 2.2x
+// at 65,536; H = 4 (6 segments) 3.4x at 32,768; H = 24 slower, so not cut.
 int32_t resolve_segments(int64_t T, int32_t H, int32_t requested, int sms, kda::SegPlan* plan)
 {
     const long long nch = (T + 63) / 64;
@@ -168,7 +168,7 @@ int32_t resolve_segments(int64_t T, int32_t H, int32_t requested, int sms, kda::
     }
     const int units_budget = sms * 8 / 25;
     int32_t G = 1;
-    while (kda::seg_units(H, G + 1) <= units_budget && nch / (G + 1) >= 48) ++G;
+    while (kda::seg_units(H, G + 1) <= units_budget && nch / (G + 1) >= 32) ++G;
     for (; G >= 2; --G)
         if (kda::seg_plan(T, H, G, sms, plan)) return G;
     return 1;

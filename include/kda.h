@@ -226,9 +226,9 @@ size_t kda_prefill_segmented_workspace_bytes(int64_t total_tokens, int32_t H,
  *              chunk and the 2 * segments - 1 chains of each head fill at
  *              most half of the SMs), or <= 0 to let the library choose: the
  *              most segments for which those chains fill about a third of
- *              the SMs and every segment has at least 48 chunks (one GB300:
+ *              the SMs and every segment has at least 32 chunks (one GB300:
  *              2 at H = 16, 3 at H = 8, 6 at H = 4; none at H >= 24 or below
- *              6,144 tokens, where cutting does not pay).
+ *              4,096 tokens, where cutting does not pay).
  *   workspace  kda_prefill_segmented_workspace_bytes(...) bytes, 256-byte
  *              aligned, not shared with concurrent calls.
  * When the shape cannot be cut (not bf16 inputs with d_k = d_v = 128, too

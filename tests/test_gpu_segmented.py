@@ -61,10 +61,19 @@ def check(kda, inp, segments, o_dtype=None):
 
 
 def test_prefill_h16_t4096_segmented(kda):
-    # the short-prompt workload: 16 heads, 64 chunks, in two segments (the
-    # automatic choice leaves it uncut: there it is on par with kda_prefill)
+    # the short-prompt workload: 16 heads, 64 chunks, in two segments
     inp = synth.workload_inputs(2, device="cpu")
     check(kda, inp, 2)
+
+
+def test_automatic_choice_cuts_the_short_prompt_in_two(kda):
+    # 64 chunks x 16 heads: two segments of 32 chunks, 48 consumer chains
+    auto = kda.kda_prefill_segmented_workspace_bytes(4096, 16, 128, 128, 0)
+    assert auto == kda.kda_prefill_segmented_workspace_bytes(4096, 16, 128, 128, 2)
+    assert auto > kda.kda_prefill_workspace_bytes(1, 16, 128, 128)
+    # 24 heads would need 72 chains: not cut
+    assert (kda.kda_prefill_segmented_workspace_bytes(4096, 24, 128, 128, 0) ==
+            kda.kda_prefill_workspace_bytes(1, 24, 128, 128))
 
 
 def test_automatic_choice_cuts_a_long_few_head_prompt(kda):
