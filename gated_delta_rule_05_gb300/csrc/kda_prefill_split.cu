@@ -527,15 +527,24 @@ __device__ __forceinline__ void producer(const Ctx& X, uint32_t tmem, int warp, 
         const int ct = t.ct;
         const int32_t* consumed = flags + (size_t)groups * R;
         int step = 0;
-        // Job jc - 1 is handed to the data-movement warp (JOB_DONE) during
-        // job jc, once pass B is done: by then ct 0's last bulk copies have
-        // completed, and the group is waiting for the Gram product anyway.
-        // It is always handed over before job jc writes its own ring slot
-        // (a later chunk of the same unit may need job jc - 1).
+        // A job's operand tiles go to its ring slot with bulk copies issued by
+        // four threads in four warps, one per staging point: ct 0 the
+        // (e^G Q)^T, Ktil^T and e^{G_last} tiles after pass B, ct 32 P after
+        // the Gram readout, ct 64 T after the solve, ct 96 -W^T after the W
+        // readout.  (Issued by one thread, a copy could hold that thread, and
+        // with it the whole group at its next barrier, while the copies
+        // before it drained.)  Each issuer waits for its own copies: for
+        // their reads of a staging tile just before the tile is written
+        // again, and for their completion before job jc - 1 is handed to
+        // the data-movement warp (JOB_DONE, four arrivals) during job jc,
+        // once pass B is done.  It is always handed over before job jc
+        // writes its own ring slot (a later chunk of the same unit may need
+        // job jc - 1).
+        const bool issuer = ct == 0 || ct == 32 || ct == 64 || ct == 96;
         auto job_done = [&](int jc_done, int npass_done) {
             bulk_wait_group0();
             fence_proxy_async_global();
-            jd[jc_done & 1].npass = npass_done;
+            if (ct == 0) jd[jc_done & 1].npass = npass_done;
             mbar_arrive(&X.bar[B_JOB_DONE]);
         };
         int prev_npass = 0;
@@ -543,8 +552,8 @@ __device__ __forceinline__ void producer(const Ctx& X, uint32_t tmem, int warp, 
             if (!group_wait(X, B_QKG_FULL, jc)) break;
             const JobDesc job = jd[jc & 1];
             if (job.terminate) {
+                if (issuer && jc > 0) job_done(jc - 1, prev_npass);
                 if (ct == 0) {
-                    if (jc > 0) job_done(jc - 1, prev_npass);
                     X.desc[step & 1].last_step = 1;
                     mbar_arrive(&X.bar[B_OPS]);        // lets the MMA warp finish
                 }
@@ -580,13 +589,14 @@ __device__ __forceinline__ void producer(const Ctx& X, uint32_t tmem, int warp, 
                 uint8_t* blk = slot + (size_t)p * kStage;
                 if (ct == 0) {
                     X.desc[step & 1].last_step = 0;
-                    bulk_wait_group_read0();       // staging areas free again
+                    bulk_wait_group_read0();       // its staging tiles free again
                 }
                 group_sync();
                 pass_factors(X, t, ps, reinterpret_cast<float*>(sm + OFF_GL));
                 gram_operands<FUSED, sizeof(TO) == 4>(X, t, ps, Gp, sm + OFF_QG, sm + OFF_KT, sm + P_GK);
                 fence_proxy_async_smem();
                 group_sync();
+                if (p == 0 && jc > 0 && issuer && ct != 0) job_done(jc - 1, prev_npass);
                 if (ct == 0) {
                     mbar_arrive(&X.bar[B_OPS]);
                     bool free_slot = true;
@@ -619,18 +629,28 @@ __device__ __forceinline__ void producer(const Ctx& X, uint32_t tmem, int warp, 
                         atomicExch(&X.misc->abort, 1);   // the group stops at its next wait
                     }
                 }
+                // Each later issuer orders its copies after ct 0's look at
+                // the slot (the group barriers in between) with a proxy
+                // fence, and lets its previous copy finish reading the
+                // staging tile before the tile is written again.
+                if (ct == 32) bulk_wait_group_read0();
                 if (!gram_readout(X, t, tmem, ps.lo, ps.hi, step, sm + OFF_P)) return false;
-                if (ct == 0) {
+                if (ct == 32) {
+                    fence_proxy_async_global();
                     bulk_store(blk + BLK_P, sm + OFF_P, 8192);
                     bulk_commit_group();
                 }
+                if (ct == 64) bulk_wait_group_read0();
                 ut_solve_mma(X, t, sm + OFF_T16);
-                if (ct == 0) {
+                if (ct == 64) {
+                    fence_proxy_async_global();
                     bulk_store(blk + BLK_T16, sm + OFF_T16, 8192);
                     bulk_commit_group();
                 }
+                if (ct == 96) bulk_wait_group_read0();
                 if (!w_readout(X, t, tmem, step, sm + OFF_WT)) return false;
-                if (ct == 0) {
+                if (ct == 96) {
+                    fence_proxy_async_global();
                     bulk_store(blk + BLK_WT, sm + OFF_WT, 16384);
                     bulk_commit_group();
                 }
@@ -649,6 +669,9 @@ __device__ __forceinline__ void producer(const Ctx& X, uint32_t tmem, int warp, 
             if (!alive) break;
             prev_npass = npass;
         }
+        // (After an abort: the copies still reading shared memory land
+        // before the CTA exits.)
+        if (issuer) bulk_wait_group0();
     }
 }
 
@@ -681,7 +704,7 @@ prefill_split_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     if (cu != nullptr && ws[kWsErrorWord] != 0) return;   // uniform: every thread returns
 
     if (tid == 0) {
-        for (int b = 0; b < kNumBars; ++b) mbar_init(&X.bar[b], 1);
+        for (int b = 0; b < kNumBars; ++b) mbar_init(&X.bar[b], b == B_JOB_DONE ? 4 : 1);
         X.misc->abort = 0;
         X.misc->wide = 0;
         fence_mbar_init();
