@@ -20,13 +20,13 @@
 // Hand-over.  Producers claim jobs (chunk c of unit u) from a 64-bit counter
 // in chunk-major order (job j = c U + u) and write the chunk's back-phase
 // operands (-W^T, (e^G Q)^T, P, Ktil^T, T as fp16 tiles in the 128-byte
-// swizzled layout of the MMA descriptors, and e^{G_last}) straight from
-// registers into slot c mod R of the unit's ring in the workspace; a chunk
-// whose decay span needs two passes fills two step blocks.  The producer's
-// data-movement warp then publishes the slot with a release store of
-// full[u][slot] = 2 (c + 1) + (passes - 1).  The consumer's loader polls that
-// word with relaxed loads and, once it shows the chunk, issues an acquire
-// fence (the relaxed load and the fence form an acquire pattern that
+// swizzled layout of the MMA descriptors, and e^{G_last}), staged in shared
+// memory, into slot c mod R of the unit's ring in the workspace with bulk
+// copies; a chunk whose decay span needs two passes fills two step blocks.
+// The producer's data-movement warp then publishes the slot with a release
+// store of full[u][slot] = 2 (c + 1) + (passes - 1).  The consumer's loader
+// polls that word with relaxed loads and, once it shows the chunk, issues an
+// acquire fence (the relaxed load and the fence form an acquire pattern that
 // synchronises with the release store) and a proxy fence, then copies each
 // step block into one of two shared-memory stages with one bulk copy.  The
 // consumer raises consumed[u] to c + 1 with a relaxed reduction once the copy
