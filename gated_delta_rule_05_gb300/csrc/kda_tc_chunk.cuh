@@ -35,10 +35,12 @@
 // with fp32 accumulation.  With fp32 output they are rounded to nearest
 // first; with bf16 output the tensor cores' truncation is left in place (its
 // bias stays well below the output's own rounding, and the rounding costs
-// several percent of the launch).  T, P, U, S, V, W, e^G Q, e^G K and Ktil are O(1) and
-// enter the tensor cores as fp16 (3 more mantissa bits than bf16).  The UT
-// solve runs in fp32 and the state is carried in fp32.  |v| and the state
-// entries are assumed to stay inside the fp16 range (|x| < 65504).
+// several percent of the launch).  T, P, U, S, V, W, e^G Q, e^G K and Ktil
+// are O(1) and enter the tensor cores as fp16 (3 more mantissa bits than
+// bf16).  The UT solve keeps about 22 significant bits (fp32 diagonal blocks,
+// two-term fp16 operands in its block products) and the state is carried in
+// fp32.  |v| and the state entries are assumed to stay inside the fp16 range
+// (|x| < 65504).
 //
 // UT solve.  X = (I + A)^{-1} by block forward substitution on 16 x 16 blocks:
 // the diagonal blocks' inverses X_bb in fp32 on the CUDA cores by column-wise
