@@ -239,8 +239,14 @@ __device__ __forceinline__ void consumer(const Ctx& X, uint32_t tmem, int warp, 
                 d.chunk = c;
                 X.desc[s] = d;
                 mbar_arrive_expect_tx(&X.bar[B_ST_FULL0 + s], kBlkBytes);
-                bulk_load(sm + s * kStage, uring + ((size_t)slot * 2 + p) * kStage, kBlkBytes,
-                          &X.bar[B_ST_FULL0 + s]);
+                // Four copies of a quarter each: one copy of the whole block
+                // streamed at about 24 bytes per cycle.
+                static_assert(kBlkBytes % 64 == 0, "quarters of 16-byte multiples");
+#pragma unroll
+                for (int qb = 0; qb < 4; ++qb)
+                    bulk_load(sm + s * kStage + qb * (kBlkBytes / 4),
+                              uring + ((size_t)slot * 2 + p) * kStage + qb * (kBlkBytes / 4),
+                              kBlkBytes / 4, &X.bar[B_ST_FULL0 + s]);
                 ++issued_st[s];
                 ++step;
             }
