@@ -109,3 +109,37 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     with pytest.raises(RuntimeError, match="not built"):
         kda.lib()
     importlib.reload(kda)
+
+
+def noalloc(lib, **kw):
+    args = dict(q=A, k=A, v=A, g=A, b=A, S0=NULL, cu=NULL, N=1, T=64, H=2, dk=128, dv=128,
+                dt=kda.KDA_BF16, o=A * 2, Sf=NULL, stream=NULL)
+    args.update(kw)
+    return lib.kda_prefill_noalloc(*args.values())
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(N=4097, cu=A * 5), kda.KDA_ERR_WORKSPACE),     # beyond the fixed scratch
+    (dict(N=0), kda.KDA_ERR_INVALID_ARG),
+])
+def test_noalloc_rejects(lib, kw, code):
+    # both are rejected before the scratch array's address is looked up
+    assert noalloc(lib, **kw) == code
+
+
+def segmented(lib, **kw):
+    args = dict(q=A, k=A, v=A, g=A, b=A, S0=NULL, T=64, H=2, dk=128, dv=128, dt=kda.KDA_BF16,
+                o=A * 2, Sf=NULL, segments=2, ws=A * 3, wsb=512, stream=NULL)
+    args.update(kw)
+    return lib.kda_prefill_segmented(*args.values())
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=NULL), kda.KDA_ERR_INVALID_ARG),
+    (dict(dk=96, dv=96), kda.KDA_ERR_UNSUPPORTED),
+    (dict(T=-1), kda.KDA_ERR_INVALID_ARG),
+    (dict(ws=NULL), kda.KDA_ERR_WORKSPACE),
+])
+def test_segmented_rejects(lib, kw, code):
+    # a single chunk cannot be cut: the call is kda_prefill, with its checks
+    assert segmented(lib, **kw) == code
